@@ -1,0 +1,175 @@
+/*
+ * wst.h -- C ABI of libwst: persistent, warp-specialized bf16 contractions
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, each one hand-written CUDA kernel behind one call:
+ *
+ *   wst_gemm_bf16            dense (optionally strided-batched) GEMM with an
+ *                            optional fused bias / bias+SiLU epilogue.
+ *                            Source: "How We Built TLX: A Hardware-Native GPU
+ *                            Compiler for Production ML at Scale" (Meta
+ *                            Engineering), section "Introducing TLX": the
+ *                            tiled matmul C = A.B with an fp32 accumulator,
+ *                            restructured into a TMA producer, a single MMA
+ *                            issuer accumulating in tensor memory, and an
+ *                            epilogue that stores the tile; the fused
+ *                            epilogue follows "Five key areas" (model-aware
+ *                            kernel fusion).
+ *   wst_grouped_gemm_bf16    one GEMM per group (mixture-of-experts expert
+ *                            matmuls) over variable, device-resident row
+ *                            offsets.  Source: same page, "TLX in
+ *                            Production" and "Case Study 3: Distributed
+ *                            Grouped GEMM for LLM Pretraining".
+ *   wst_ikbo_linear_compress in-kernel-broadcast linear compression,
+ *                            Y[c] = W . concat(U[user(c)], Cf[c]), with the
+ *                            user part W_u.U[u] computed once per user and
+ *                            broadcast inside the kernel.  Source: same page,
+ *                            "Case Study 2: In-Kernel Broadcast Optimization
+ *                            for RecSys" and "TLX Provides a Building Block
+ *                            for the Final Stage of This Optimization"
+ *                            (matmul decomposition, a persistent
+ *                            warp-specialized kernel in which user and
+ *                            candidate GEMMs share one buffer ring, and
+ *                            tile-level release/acquire across CTAs).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All matrix pointers are DEVICE pointers to memory the caller owns and
+ *    keeps alive until the work on `stream` has finished.  The library never
+ *    allocates, frees or keeps device memory of its own, and never falls back
+ *    to the CPU.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is asynchronous: it validates its arguments on the host, enqueues
+ *    one kernel on `stream`, and returns.
+ *  - bf16 is IEEE-style bfloat16; accumulation is fp32; bf16 outputs are
+ *    rounded to nearest even.
+ *  - Alignment: every matrix pointer is 16-byte aligned and every leading
+ *    dimension / batch stride, in bytes, is a multiple of 16 (the tensor
+ *    memory accelerator's rule).  Otherwise WST_ERR_ALIGNMENT.
+ *  - `workspace` is a caller-owned device buffer of at least
+ *    wst_workspace_size(...) bytes, zero-filled once before first use (for
+ *    example with wst_workspace_init).  It carries the device error word and,
+ *    for IKBO, the per-user partial products and their ready flags.  One
+ *    workspace must not be used by two calls that can run at the same time.
+ *  - Errors found on the host are returned before anything is enqueued.
+ *    Errors found on the device (a bounded wait that ran out, inconsistent
+ *    device offsets) are latched in the workspace; wst_sync_status reads and
+ *    clears them.  No call aborts, traps or throws.
+ */
+#ifndef WST_H_
+#define WST_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WST_OK = 0,
+  WST_ERR_INVALID_ARG = 1,  /* a size, pointer, stride or enum is out of range   */
+  WST_ERR_ALIGNMENT = 2,    /* pointer / stride breaks the 16-byte rule          */
+  WST_ERR_UNSUPPORTED = 3,  /* valid request this build does not implement        */
+  WST_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (see message)    */
+  WST_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out                 */
+  WST_ERR_BAD_OFFSETS = 6   /* device offsets not non-decreasing from 0 to total  */
+} wst_status;
+
+typedef enum { WST_F32 = 0, WST_BF16 = 1 } wst_dtype;
+
+typedef enum {
+  WST_EPI_NONE = 0,      /* C = A.B^T                                   */
+  WST_EPI_BIAS = 1,      /* C = A.B^T + bias[n]                         */
+  WST_EPI_BIAS_SILU = 2  /* C = SiLU(A.B^T + bias[n]), SiLU(x)=x/(1+e^-x) */
+} wst_epilogue;
+
+/* Bytes of workspace a call needs.  GEMM and grouped GEMM need
+ * wst_workspace_size(0, 0, 0); IKBO needs wst_workspace_size(num_users, O, D). */
+size_t wst_workspace_size(int num_users, int O, int D);
+
+/* Zero-fill `bytes` of `workspace` on `stream` (asynchronous). */
+wst_status wst_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * Dense / strided-batched GEMM.  For b in [0,batch), m in [0,M), n in [0,N):
+ *   C[b][m][n] = epi( sum_k A[b][m][k] * B[b][n][k] (+ bias[b][n]) )
+ *   A     bf16, element (b,m,k) at A + b*strideA + m*lda + k   (row-major M x K)
+ *   B     bf16, element (b,n,k) at B + b*strideB + n*ldb + k   (N x K, K
+ *         contiguous: the column-major K x N operand)
+ *   bias  bf16, element (b,n) at bias + b*strideBias + n; NULL unless epi>0;
+ *         strideBias 0 shares one bias row across the batch
+ *   C     c_type, element (b,m,n) at C + b*strideC + m*ldc + n
+ *   Strides are in ELEMENTS.  strideA / strideB may be 0 (operand shared by
+ *   the whole batch); strideC must be 0 only when batch == 1.
+ * Requires batch >= 1, M, N, K >= 1, lda >= K, ldb >= K, ldc >= N.
+ */
+wst_status wst_gemm_bf16(int batch, int M, int N, int K,
+                         const void* A, long lda, long strideA,
+                         const void* B, long ldb, long strideB,
+                         const void* bias, long strideBias,
+                         void* C, long ldc, long strideC, wst_dtype c_type,
+                         wst_epilogue epi, void* workspace, void* stream);
+
+/*
+ * Grouped GEMM over G groups sharing N and K.  d_offsets is a DEVICE int32
+ * array of G+1 entries, non-decreasing, d_offsets[0] = 0, d_offsets[G] =
+ * M_total; group g owns rows [d_offsets[g], d_offsets[g+1]) of A and C
+ * (empty groups allowed):
+ *   C[m][n] = epi( sum_k A[m][k] * B[g][n][k] (+ bias[g][n]) ),  m in group g
+ *   A     bf16 [M_total][K] row-major, leading dimension lda
+ *   B     bf16, element (g,n,k) at B + g*strideB_group + n*ldb + k
+ *   bias  bf16, element (g,n) at bias + g*strideBias + n, or NULL (epi == 0)
+ *   C     c_type [M_total][N], leading dimension ldc.  Rows outside every
+ *         group are never written.
+ * Offsets that break the rule are detected on the device: the kernel clamps
+ * them into [0, M_total] (so no access leaves the buffers) and latches
+ * WST_ERR_BAD_OFFSETS for wst_sync_status.
+ */
+wst_status wst_grouped_gemm_bf16(int G, int M_total, int N, int K,
+                                 const void* A, long lda,
+                                 const void* B, long ldb, long strideB_group,
+                                 const int* d_offsets,
+                                 const void* bias, long strideBias,
+                                 void* C, long ldc, wst_dtype c_type,
+                                 wst_epilogue epi, void* workspace, void* stream);
+
+/*
+ * IKBO linear compression.  Candidates of user u are [off[u], off[u+1]) of
+ * the DEVICE int32 array d_user_offsets (num_users+1 entries, non-decreasing,
+ * from 0 to num_cand).  For every candidate c of user u:
+ *   Y[c][o][d] = sum_{f<Du} W[o][f] U[u][f][d] + sum_{f<Dc} W[o][Du+f] Cf[c][f][d]
+ *   U   bf16 [num_users][Du][D]   (d contiguous)
+ *   Cf  bf16 [num_cand][Dc][D]    (d contiguous)
+ *   W   bf16 [O][Du+Dc]           (user columns first)
+ *   Y   fp32 [num_cand][O][D]     (d contiguous)
+ * The user part P[u] = W[:, :Du].U[u] is computed once per user per call
+ * into the workspace and added to each of that user's candidates inside the
+ * kernel; the broadcast user features are never materialised.
+ * This build supports D == 128, O a multiple of 32 up to 256, Du and Dc
+ * multiples of 8 with Du + Dc <= 512 (else WST_ERR_UNSUPPORTED).  The
+ * kernel is a cooperative launch: all of its CTAs are resident at once.
+ */
+wst_status wst_ikbo_linear_compress(int num_users, int num_cand, int Du, int Dc,
+                                    int D, int O,
+                                    const void* U, const void* Cf, const void* W,
+                                    const int* d_user_offsets,
+                                    void* Y, void* workspace, void* stream);
+
+/* Synchronize `stream`, then return and clear the first device-side error
+ * latched in `workspace` (WST_OK if none). */
+wst_status wst_sync_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* wst_status_string(wst_status s);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* wst_last_error(void);
+
+/* Library version string. */
+const char* wst_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WST_H_ */

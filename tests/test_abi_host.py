@@ -1,0 +1,96 @@
+"""Host-only checks of the C ABI (no GPU, no compute call): the library
+builds and loads, exports every function include/wst.h declares, and rejects
+invalid arguments with the documented status before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import warp_specialized_tensor_gb300 as wst
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return wst.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "wst.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(wst_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), "libwst.so does not export %s" % n
+
+
+def test_status_strings_and_version(lib):
+    for code in range(7):
+        s = wst.wst_status_string(code)
+        assert s.startswith("WST_")
+    assert "sm_103a" in wst.wst_version()
+
+
+def test_workspace_sizes(lib):
+    assert wst.wst_workspace_size(0, 0, 0) == 256
+    # header + 64 flags padded to 256 B + 64*32*128 fp32 partials
+    assert wst.wst_workspace_size(64, 32, 128) == 256 + 256 + 64 * 32 * 128 * 4
+    assert wst.wst_workspace_size(65, 32, 128) == 256 + 512 + 65 * 32 * 128 * 4
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def gemm(lib, **kw):
+    a = dict(batch=1, M=128, N=128, K=64, A=FAKE, lda=64, sA=0, B=FAKE, ldb=64, sB=0,
+             bias=None, sBias=0, C=FAKE, ldc=128, sC=0, ct=1, epi=0, ws=FAKE, st=None)
+    a.update(kw)
+    return lib.wst_gemm_bf16(a["batch"], a["M"], a["N"], a["K"], a["A"], a["lda"], a["sA"],
+                             a["B"], a["ldb"], a["sB"], a["bias"], a["sBias"], a["C"], a["ldc"],
+                             a["sC"], a["ct"], a["epi"], a["ws"], a["st"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), wst.WST_ERR_INVALID_ARG),
+    (dict(K=-1), wst.WST_ERR_INVALID_ARG),
+    (dict(batch=0), wst.WST_ERR_INVALID_ARG),
+    (dict(A=None), wst.WST_ERR_INVALID_ARG),
+    (dict(ws=None), wst.WST_ERR_INVALID_ARG),
+    (dict(lda=32), wst.WST_ERR_INVALID_ARG),
+    (dict(epi=7), wst.WST_ERR_INVALID_ARG),
+    (dict(ct=5), wst.WST_ERR_INVALID_ARG),
+    (dict(epi=1), wst.WST_ERR_INVALID_ARG),            # bias missing
+    (dict(A=FAKE + 8), wst.WST_ERR_ALIGNMENT),
+    (dict(lda=68), wst.WST_ERR_ALIGNMENT),             # 136 B rows
+    (dict(N=100, ldc=100), wst.WST_ERR_ALIGNMENT),     # 200 B rows of bf16
+    (dict(batch=2, sC=10), wst.WST_ERR_INVALID_ARG),   # overlapping outputs
+    (dict(), wst.WST_ERR_INVALID_ARG),                 # not device memory (no GPU here)
+])
+def test_gemm_rejects(lib, kw, code):
+    assert gemm(lib, **kw) == code
+    assert lib.wst_last_error().decode() != ""
+
+
+def test_grouped_and_ikbo_reject(lib):
+    g = lib.wst_grouped_gemm_bf16
+    assert g(0, 10, 128, 64, FAKE, 64, FAKE, 64, 0, FAKE, None, 0, FAKE, 128, 1, 0, FAKE, None) == wst.WST_ERR_INVALID_ARG
+    assert g(2, 10, 128, 64, FAKE, 64, FAKE, 64, 0, FAKE + 2, None, 0, FAKE, 128, 1, 0, FAKE, None) == wst.WST_ERR_ALIGNMENT
+    assert g(2, 10, 128, 64, FAKE, 64, FAKE, 64, 0, None, None, 0, FAKE, 128, 1, 0, FAKE, None) == wst.WST_ERR_INVALID_ARG
+    k = lib.wst_ikbo_linear_compress
+    args = [64, 8192, 256, 64, 128, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None]
+    bad = list(args); bad[4] = 96      # D != 128
+    assert k(*bad) == wst.WST_ERR_UNSUPPORTED
+    bad = list(args); bad[5] = 48      # O not a multiple of 32
+    assert k(*bad) == wst.WST_ERR_UNSUPPORTED
+    bad = list(args); bad[2] = 250     # Du not a multiple of 8
+    assert k(*bad) == wst.WST_ERR_UNSUPPORTED
+    bad = list(args); bad[0] = 0
+    assert k(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[6] = FAKE + 4
+    assert k(*bad) == wst.WST_ERR_ALIGNMENT

@@ -1,0 +1,249 @@
+"""Python binding of libwst, the GB300 (sm_103a) warp-specialized contraction
+library.  Argument marshalling only: every step of the computation runs in the
+CUDA kernels behind the C ABI declared in ``include/wst.h``; there is no CPU
+or PyTorch fallback.  PyTorch supplies device memory and streams.
+
+The functions carry the C ABI's names and take torch tensors; sizes, leading
+dimensions and batch strides are read from the tensors' shapes and strides.
+A non-OK status raises :class:`WstError`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "F32", "BF16",
+    "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
+    "workspace", "wst_gemm_bf16", "wst_grouped_gemm_bf16",
+    "wst_ikbo_linear_compress", "wst_sync_status", "wst_status_string",
+    "wst_version",
+]
+
+# enums of include/wst.h
+WST_OK, WST_ERR_INVALID_ARG, WST_ERR_ALIGNMENT, WST_ERR_UNSUPPORTED = 0, 1, 2, 3
+WST_ERR_CUDA, WST_ERR_TIMEOUT, WST_ERR_BAD_OFFSETS = 4, 5, 6
+F32, BF16 = 0, 1
+EPI_NONE, EPI_BIAS, EPI_BIAS_SILU = 0, 1, 2
+_EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_silu": EPI_BIAS_SILU}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class WstError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__("%s: %s%s" % (where, wst_status_string(status),
+                                       (" -- " + detail) if detail else ""))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libwst.so (building it in-tree with nvcc when absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise ImportError("libwst.so is not built; run warp_specialized_tensor_gb300._build.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        P, I, L, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_size_t
+        lib.wst_workspace_size.argtypes = [I, I, I]
+        lib.wst_workspace_size.restype = Z
+        lib.wst_workspace_init.argtypes = [P, Z, P]
+        lib.wst_workspace_init.restype = I
+        lib.wst_gemm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, P, L, P, L, L, I, I, P, P]
+        lib.wst_gemm_bf16.restype = I
+        lib.wst_grouped_gemm_bf16.argtypes = [I, I, I, I, P, L, P, L, L, P, P, L, P, L, I, I, P, P]
+        lib.wst_grouped_gemm_bf16.restype = I
+        lib.wst_ikbo_linear_compress.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
+        lib.wst_ikbo_linear_compress.restype = I
+        lib.wst_sync_status.argtypes = [P, P]
+        lib.wst_sync_status.restype = I
+        lib.wst_status_string.argtypes = [I]
+        lib.wst_status_string.restype = ctypes.c_char_p
+        lib.wst_last_error.argtypes = []
+        lib.wst_last_error.restype = ctypes.c_char_p
+        lib.wst_version.argtypes = []
+        lib.wst_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def wst_status_string(status: int) -> str:
+    return load_library().wst_status_string(int(status)).decode()
+
+
+def wst_version() -> str:
+    return load_library().wst_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != WST_OK:
+        detail = load_library().wst_last_error().decode()
+        raise WstError(status, where, detail)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _epi(epi) -> int:
+    return _EPI_NAMES[epi] if isinstance(epi, str) else int(epi)
+
+
+def _ctype(C) -> int:
+    if C.dtype == torch.float32:
+        return F32
+    if C.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("C must be float32 or bfloat16")
+
+
+def _need(t, name, dtype=None, dims=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s" % (name, dtype))
+    if dims is not None and t.dim() not in dims:
+        raise ValueError("%s must have %s dimensions" % (name, dims))
+    if t.stride(-1) != 1:
+        raise ValueError("%s must have a contiguous last dimension" % name)
+
+
+# ----------------------------------------------------------------------------
+# workspace
+# ----------------------------------------------------------------------------
+def wst_workspace_size(num_users: int = 0, O: int = 0, D: int = 0) -> int:
+    return int(load_library().wst_workspace_size(num_users, O, D))
+
+
+def wst_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(load_library().wst_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(),
+                                             _stream_handle(stream)), "wst_workspace_init")
+
+
+def workspace(num_users: int = 0, O: int = 0, D: int = 0, device=None, stream=None) -> torch.Tensor:
+    """Allocate (through PyTorch) and zero-fill a workspace for these sizes."""
+    n = wst_workspace_size(num_users, O, D)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    wst_workspace_init(ws, stream)
+    return ws
+
+
+# ----------------------------------------------------------------------------
+# the three operations
+# ----------------------------------------------------------------------------
+def wst_gemm_bf16(A, B, C, bias=None, epi="none", workspace=None, stream=None) -> None:
+    """C[b] = epi(A[b] . B[b]^T (+ bias[b])) on the GPU.
+
+    A: bf16 [M,K] or [batch,M,K]; B: bf16 [N,K] or [batch,N,K] (a 2-D B is
+    shared by the batch); C: bf16/fp32 [M,N] or [batch,M,N]; bias: bf16 [N]
+    (shared) or [batch,N]."""
+    _need(A, "A", torch.bfloat16, (2, 3))
+    _need(B, "B", torch.bfloat16, (2, 3))
+    _need(C, "C", None, (2, 3))
+    if workspace is None:
+        raise ValueError("workspace is required (see workspace())")
+    batch = A.shape[0] if A.dim() == 3 else 1
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-2]
+    if B.shape[-1] != K or C.shape[-2:] != (M, N):
+        raise ValueError("shape mismatch: A %s B %s C %s" % (tuple(A.shape), tuple(B.shape), tuple(C.shape)))
+    if C.dim() == 3 and C.shape[0] != batch:
+        raise ValueError("C batch mismatch")
+    sA = A.stride(0) if A.dim() == 3 else 0
+    sB = B.stride(0) if B.dim() == 3 else 0
+    if B.dim() == 3 and B.shape[0] != batch:
+        raise ValueError("B batch mismatch")
+    sC = C.stride(0) if C.dim() == 3 else 0
+    e = _epi(epi)
+    sBias = 0
+    if e != EPI_NONE:
+        _need(bias, "bias", torch.bfloat16, (1, 2))
+        sBias = bias.stride(0) if bias.dim() == 2 else 0
+    st = load_library().wst_gemm_bf16(
+        batch, M, N, K, A.data_ptr(), A.stride(-2), sA, B.data_ptr(), B.stride(-2), sB,
+        _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(-2), sC, _ctype(C), e,
+        workspace.data_ptr(), _stream_handle(stream))
+    _check(st, "wst_gemm_bf16")
+
+
+def wst_grouped_gemm_bf16(A, B, offsets, C, bias=None, epi="none", workspace=None,
+                          stream=None) -> None:
+    """Rows [off[g], off[g+1]) of C = epi(rows of A . B[g]^T (+ bias[g])).
+
+    A: bf16 [M_total,K]; B: bf16 [G,N,K]; offsets: device int32 [G+1];
+    C: bf16/fp32 [M_total,N]; bias: bf16 [G,N]."""
+    _need(A, "A", torch.bfloat16, (2,))
+    _need(B, "B", torch.bfloat16, (3,))
+    _need(C, "C", None, (2,))
+    _need(offsets, "offsets", torch.int32, (1,))
+    if workspace is None:
+        raise ValueError("workspace is required (see workspace())")
+    G, N, K = B.shape
+    M_total = A.shape[0]
+    if A.shape[1] != K or C.shape != (M_total, N) or offsets.numel() != G + 1:
+        raise ValueError("shape mismatch")
+    e = _epi(epi)
+    sBias = 0
+    if e != EPI_NONE:
+        _need(bias, "bias", torch.bfloat16, (2,))
+        sBias = bias.stride(0)
+    st = load_library().wst_grouped_gemm_bf16(
+        G, M_total, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(1), B.stride(0),
+        offsets.data_ptr(), _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(0),
+        _ctype(C), e, workspace.data_ptr(), _stream_handle(stream))
+    _check(st, "wst_grouped_gemm_bf16")
+
+
+def wst_ikbo_linear_compress(U, Cf, W, user_offsets, Y, workspace, stream=None) -> None:
+    """Y[c] = W . concat(U[user(c)], Cf[c]) with the user part computed once per user.
+
+    U: bf16 [users,Du,D]; Cf: bf16 [cand,Dc,D]; W: bf16 [O,Du+Dc];
+    user_offsets: device int32 [users+1]; Y: fp32 [cand,O,D]; workspace of
+    wst_workspace_size(users, O, D) bytes."""
+    for t, n, d in ((U, "U", 3), (Cf, "Cf", 3), (W, "W", 2)):
+        _need(t, n, torch.bfloat16, (d,))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    _need(Y, "Y", torch.float32, (3,))
+    _need(user_offsets, "user_offsets", torch.int32, (1,))
+    if not Y.is_contiguous():
+        raise ValueError("Y must be contiguous")
+    users, Du, D = U.shape
+    cand, Dc, D2 = Cf.shape
+    O, F = W.shape
+    if D2 != D or F != Du + Dc or Y.shape != (cand, O, D) or user_offsets.numel() != users + 1:
+        raise ValueError("shape mismatch")
+    need = wst_workspace_size(users, O, D)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError("workspace too small: %d < %d bytes" % (workspace.numel(), need))
+    st = load_library().wst_ikbo_linear_compress(
+        users, cand, Du, Dc, D, O, U.data_ptr(), Cf.data_ptr(), W.data_ptr(),
+        user_offsets.data_ptr(), Y.data_ptr(), workspace.data_ptr(), _stream_handle(stream))
+    _check(st, "wst_ikbo_linear_compress")
+
+
+def wst_sync_status(workspace, stream=None) -> int:
+    """Synchronize the stream; return (and clear) the first device-side error code."""
+    return int(load_library().wst_sync_status(workspace.data_ptr(), _stream_handle(stream)))

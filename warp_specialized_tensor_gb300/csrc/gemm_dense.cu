@@ -1,0 +1,16 @@
+// gemm_dense.cu -- dense / strided-batched instantiations of the
+// warp-specialized GEMM, and the entry used by the C ABI.
+#include "gemm_ws_launch.cuh"
+
+namespace wst {
+
+int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream);
+
+int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
+  DeviceInfo dev;
+  int st = current_device_info(&dev);
+  if (st) return st;
+  return pr.grouped ? run_gemm_grouped(pr, dev, stream) : dispatch<false>(pr, dev, stream);
+}
+
+}  // namespace wst

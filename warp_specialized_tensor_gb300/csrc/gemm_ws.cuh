@@ -1,0 +1,474 @@
+// gemm_ws.cuh -- persistent, warp-specialized bf16 GEMM for sm_103a.
+//
+// One kernel template serves the dense / strided-batched GEMM and the
+// grouped (mixture-of-experts) GEMM.  Per CTA (one per SM, persistent):
+//
+//   warp 0      TMA producer: one thread streams A and B K-blocks (64 bf16 =
+//               128 B rows, 128-byte swizzle) into a STAGES-deep shared-memory
+//               ring; full[s] carries the transaction bytes, empty[s] is
+//               released by the MMA completion.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (128 x BN x 16,
+//               bf16 -> fp32) into one of two tensor-memory accumulators and
+//               commits completion to empty[s] (ring slot free) and, after the
+//               last K-block of a tile, to acc_full[a].
+//   warp 2      allocates / frees the tensor memory (2 x BN columns).
+//   warps 4..   epilogue: wait acc_full[a], tcgen05.ld 32 columns at a time,
+//               optional bias / SiLU, fp32 -> bf16 (RNE) or fp32, stage in a
+//               swizzled per-warp shared buffer and TMA-store it; then
+//               release acc_empty[a].  Two accumulators let the epilogue of
+//               tile i overlap the MMAs of tile i+1.
+//
+// This is the Blackwell matmul of "How We Built TLX: A Hardware-Native GPU
+// Compiler for Production ML at Scale" (Meta Engineering), section
+// "Introducing TLX" (producer / MMA / epilogue roles, NUM_STAGES ring with
+// load and dot barriers, TMEM accumulator, use_acc = k > 0), made persistent
+// ("TLX Provides a Building Block ...": one persistent kernel, ping-pong
+// between consumers) and extended to variable-size groups for expert
+// matmuls ("Case Study 3: Distributed Grouped GEMM for LLM Pretraining").
+#pragma once
+
+#include "wst_common.cuh"
+
+namespace wst {
+
+constexpr int kBM = 128;     // tile rows (TMEM lanes)
+constexpr int kBK = 64;      // K-block: 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;   // K per tcgen05.mma (kind::f16)
+
+struct GemmArgs {
+  int batch, M, N, K;
+  int m_tiles, n_tiles, k_blocks;
+  long long tiles_total;  // dense only
+  int group_m;            // raster: m-tiles per band
+  int a3d, b3d, c3d;      // operand maps carry a batch / group coordinate
+  const __nv_bfloat16* bias;
+  long long bias_stride;
+  void* C;                // for masked stores of partial group tiles
+  long long ldc;
+  const int* offsets;     // grouped: device int32[G+1]
+  int G, M_total;
+  WsHeader* ws;
+  unsigned long long timeout_ns;
+};
+
+struct Tile {
+  int b;        // batch (dense) or group (grouped)
+  int m0;       // first row (absolute row of A / C)
+  int n0;       // first column
+  int row_end;  // rows >= row_end are not part of this tile's problem
+};
+
+// --------------------------------------------------------------------------
+// schedulers
+// --------------------------------------------------------------------------
+template <int BN>
+__device__ __forceinline__ Tile dense_tile(const GemmArgs& p, long long t) {
+  const long long per_batch = (long long)p.m_tiles * p.n_tiles;
+  const int b = (int)(t / per_batch);
+  const int r = (int)(t - (long long)b * per_batch);
+  // Banded raster: group_m consecutive m-tiles sweep all n-tiles together,
+  // so a wave of CTAs shares A rows and B columns in L2.
+  const int band = p.group_m * p.n_tiles;
+  const int bi = r / band;
+  const int first_m = bi * p.group_m;
+  const int rows = min(p.group_m, p.m_tiles - first_m);
+  const int rr = r - bi * band;
+  const int m = first_m + rr % rows;
+  const int n = rr / rows;
+  return Tile{b, m * kBM, n * BN, p.M};
+}
+
+// Walks the groups in order; every role of a CTA runs its own walker over
+// the same increasing tile indices, so they agree on the sequence.
+struct GroupWalker {
+  int g;            // current group
+  long long base;   // first global tile index of group g
+  long long count;  // tiles in group g
+  int row0, row1;   // clamped rows of group g
+  int mt;           // m-tiles of group g
+
+  __device__ __forceinline__ void load(const GemmArgs& p, int n_tiles) {
+    if (g >= p.G) { count = 0; return; }
+    int a = __ldg(p.offsets + g);
+    int b = __ldg(p.offsets + g + 1);
+    a = min(max(a, 0), p.M_total);
+    b = min(max(b, a), p.M_total);
+    row0 = a;
+    row1 = b;
+    mt = (b - a + kBM - 1) / kBM;
+    count = (long long)mt * n_tiles;
+  }
+  __device__ __forceinline__ void init(const GemmArgs& p, int n_tiles) {
+    g = 0;
+    base = 0;
+    load(p, n_tiles);
+  }
+  // Advance to the group holding tile t; false when t is past the last tile.
+  __device__ __forceinline__ bool seek(const GemmArgs& p, int n_tiles, long long t) {
+    while (g < p.G && t >= base + count) {
+      base += count;
+      ++g;
+      load(p, n_tiles);
+    }
+    return g < p.G;
+  }
+  template <int BN>
+  __device__ __forceinline__ Tile tile(long long t) const {
+    const int r = (int)(t - base);
+    const int m = r % mt;  // m-minor: consecutive tiles share the expert's B columns
+    const int n = r / mt;
+    return Tile{g, row0 + m * kBM, n * BN, row1};
+  }
+};
+
+// One pass over all offsets by one thread: latch kErrBadOffsets if they are
+// not non-decreasing from 0 to M_total.
+static __device__ __noinline__ void check_offsets(const GemmArgs& p) {
+  bool bad = __ldg(p.offsets) != 0 || __ldg(p.offsets + p.G) != p.M_total;
+  int prev = 0;
+  for (int g = 0; g <= p.G && !bad; ++g) {
+    int v = __ldg(p.offsets + g);
+    if (v < prev || v > p.M_total) bad = true;
+    prev = v;
+  }
+  if (bad) latch_error(p.ws, kErrBadOffsets, 0);
+}
+
+// --------------------------------------------------------------------------
+// epilogue helpers
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float silu_f(float x) {
+  // x * sigmoid(x); __expf overflows to +inf for very negative x, giving -0.
+  return __fdividef(x, 1.0f + __expf(-x));
+}
+
+template <int EPI>
+__device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat16* bias_row,
+                                               int col, int N) {
+  if constexpr (EPI == 0) {
+    return;
+  } else {
+    if (col + 32 <= N) {
+      const uint4* bp = reinterpret_cast<const uint4*>(bias_row + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w = __ldg(bp + q);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(h[e]);
+          v[q * 8 + e * 2] += f.x;
+          v[q * 8 + e * 2 + 1] += f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col + j < N) v[j] += __bfloat162float(bias_row[col + j]);
+    }
+    if constexpr (EPI == 2) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// the kernel
+// --------------------------------------------------------------------------
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED>
+struct GemmCfg {
+  static constexpr int kThreads = 128 + 32 * EPI_WARPS;
+  static constexpr int kABytes = kBM * kBK * 2;        // 16 KB
+  static constexpr int kBBytes = BN * kBK * 2;         // 32 KB at BN = 256
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStageBufs = EPI_WARPS == 4 ? 2 : 1;  // staging buffers per epilogue warp
+  static constexpr int kStgBytes = 32 * 128;           // 32 rows x 128 B
+  static constexpr int kColsPerChunk = OUT_F32 ? 32 : 64;
+  static constexpr int kWarpCols = BN / (EPI_WARPS / 4);  // columns one epilogue warp drains
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr size_t kSmemBytes = (size_t)STAGES * kStageBytes +
+                                       (size_t)EPI_WARPS * kStageBufs * kStgBytes + 256 /*bars*/ +
+                                       1024 /*alignment slack*/;
+  static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kWarpCols % kColsPerChunk == 0, "epilogue chunking");
+};
+
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED>
+__global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
+    k_gemm_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
+  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, GROUPED>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES * Cfg::kABytes;
+  uint8_t* smStg = smB + STAGES * Cfg::kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smStg + EPI_WARPS * Cfg::kStageBufs * Cfg::kStgBytes);
+  // bars: full[STAGES] | empty[STAGES] | acc_full[2] | acc_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t bar_base = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), EPI_WARPS);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 2) {
+    tmem_alloc<1>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const Guard guard{p.ws, abort_flag, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      if (GROUPED && blockIdx.x == 0) check_offsets(p);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      GroupWalker gw;
+      if (GROUPED) gw.init(p, p.n_tiles);
+      for (long long t = blockIdx.x; ok; t += gridDim.x) {
+        Tile tl;
+        if constexpr (GROUPED) {
+          if (!gw.seek(p, p.n_tiles, t)) break;
+          tl = gw.tile<BN>(t);
+        } else {
+          if (t >= p.tiles_total) break;
+          tl = dense_tile<BN>(p, t);
+        }
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+          const uint32_t dA = smem_addr(smA + stage * Cfg::kABytes);
+          const uint32_t dB = smem_addr(smB + stage * Cfg::kBBytes);
+          const int kx = kb * kBK;
+          if (p.a3d) tma_load_3d(dA, &tmA, full_bar(stage), kx, tl.m0, tl.b);
+          else       tma_load_2d(dA, &tmA, full_bar(stage), kx, tl.m0);
+          if (p.b3d) tma_load_3d(dB, &tmB, full_bar(stage), kx, tl.n0, tl.b);
+          else       tma_load_2d(dB, &tmB, full_bar(stage), kx, tl.n0);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Drain: every slot released => every MMA that read the ring completed.
+      for (int i = 0; i < STAGES && ok; ++i) {
+        ok = wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | 0x100 | stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      GroupWalker gw;
+      if (GROUPED) gw.init(p, p.n_tiles);
+      for (long long t = blockIdx.x; ok; t += gridDim.x) {
+        if constexpr (GROUPED) {
+          if (!gw.seek(p, p.n_tiles, t)) break;
+        } else {
+          if (t >= p.tiles_total) break;
+        }
+        if (!wait_phase(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase(guard, full_bar(stage), phase, (kRoleMma << 16) | stage)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t aBase = smem_addr(smA + stage * Cfg::kABytes);
+          const uint32_t bBase = smem_addr(smB + stage * Cfg::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sdesc_sw128(aBase + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(bBase + k * 32, 16, 1024);
+            umma_bf16<1>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));  // slot free once these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(acc));  // accumulator complete
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int ew = warp - 4;              // 0 .. EPI_WARPS-1
+    const int q = warp & 3;               // TMEM lane quadrant this warp may access
+    const int col_begin = (ew >> 2) * Cfg::kWarpCols;
+    uint8_t* stg = smStg + ew * Cfg::kStageBufs * Cfg::kStgBytes;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int buf = 0;
+    GroupWalker gw;
+    if (GROUPED) gw.init(p, p.n_tiles);
+    for (long long t = blockIdx.x;; t += gridDim.x) {
+      Tile tl;
+      if constexpr (GROUPED) {
+        if (!gw.seek(p, p.n_tiles, t)) break;
+        tl = gw.tile<BN>(t);
+      } else {
+        if (t >= p.tiles_total) break;
+        tl = dense_tile<BN>(p, t);
+      }
+      if (!warp_wait_phase(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc)) break;
+      tc_fence_after_sync();
+
+      const int row_base = tl.m0 + q * 32;  // first row this warp drains
+      const int row = row_base + (int)lane;
+      const bool full_rows = !GROUPED || (row_base + 32 <= tl.row_end);
+      const __nv_bfloat16* bias_row =
+          EPI ? p.bias + (long long)tl.b * p.bias_stride : nullptr;
+      const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+
+#pragma unroll 1
+      for (int c0 = col_begin; c0 < col_begin + Cfg::kWarpCols; c0 += Cfg::kColsPerChunk) {
+        float v0[32];
+        tmem_load32(t_lane + c0, v0);
+        apply_bias_act<EPI>(v0, bias_row, tl.n0 + c0, p.N);
+        uint32_t packed[16];
+        float v1[32];
+        if constexpr (!OUT_F32) {
+          tmem_load32(t_lane + c0 + 32, v1);
+          apply_bias_act<EPI>(v1, bias_row, tl.n0 + c0 + 32, p.N);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+        }
+        // Chunks that start past the last row / column store nothing (a TMA
+        // store is never issued at an out-of-range start coordinate).
+        const bool chunk_live = row_base < tl.row_end && tl.n0 + c0 < p.N;
+        if (!chunk_live) {
+          // nothing to store
+        } else if (full_rows) {
+          // Stage the 32 x 128 B block (128-byte swizzle) and TMA-store it.
+          uint8_t* sb = stg + buf * Cfg::kStgBytes;
+          if (Cfg::kStageBufs == 2) {
+            if (lane == 0) bulk_wait_group_read<1>();
+          } else {
+            if (lane == 0) bulk_wait_group_read<0>();
+          }
+          __syncwarp();
+          const uint32_t row_addr = smem_addr(sb) + lane * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t dst = row_addr + ((uint32_t)(j ^ (lane & 7)) << 4);
+            if constexpr (OUT_F32) {
+              st_shared_v4(dst, __float_as_uint(v0[4 * j]), __float_as_uint(v0[4 * j + 1]),
+                           __float_as_uint(v0[4 * j + 2]), __float_as_uint(v0[4 * j + 3]));
+            } else {
+              uint32_t w0, w1, w2, w3;
+              if (j < 4) {
+                w0 = packed[4 * j]; w1 = packed[4 * j + 1]; w2 = packed[4 * j + 2]; w3 = packed[4 * j + 3];
+              } else {
+                const int jj = j - 4;
+                w0 = pack_bf16x2(v1[8 * jj], v1[8 * jj + 1]);
+                w1 = pack_bf16x2(v1[8 * jj + 2], v1[8 * jj + 3]);
+                w2 = pack_bf16x2(v1[8 * jj + 4], v1[8 * jj + 5]);
+                w3 = pack_bf16x2(v1[8 * jj + 6], v1[8 * jj + 7]);
+              }
+              st_shared_v4(dst, w0, w1, w2, w3);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (p.c3d) tma_store_3d(&tmC, smem_addr(sb), tl.n0 + c0, row_base, tl.b);
+            else       tma_store_2d(&tmC, smem_addr(sb), tl.n0 + c0, row_base);
+            bulk_commit_group();
+          }
+          if (Cfg::kStageBufs == 2) buf ^= 1;
+        } else if (row < tl.row_end) {
+          // Partial group tile: rows past the group end belong to the next
+          // group and must not be written.  Masked direct stores.
+          const int colg = tl.n0 + c0;
+          if constexpr (OUT_F32) {
+            float* crow = reinterpret_cast<float*>(p.C) + (long long)row * p.ldc;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int cc = colg + 4 * j;
+              if (cc + 4 <= p.N) {
+                *reinterpret_cast<float4*>(crow + cc) =
+                    make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+              } else {
+                for (int e = 0; e < 4; ++e)
+                  if (cc + e < p.N) crow[cc + e] = v0[4 * j + e];
+              }
+            }
+          } else {
+            __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int cc = colg + 8 * j;
+              const float* src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+              if (cc + 8 <= p.N) {
+                uint4 w;
+                w.x = pack_bf16x2(src[0], src[1]);
+                w.y = pack_bf16x2(src[2], src[3]);
+                w.z = pack_bf16x2(src[4], src[5]);
+                w.w = pack_bf16x2(src[6], src[7]);
+                *reinterpret_cast<uint4*>(crow + cc) = w;
+              } else {
+                for (int e = 0; e < 8; ++e)
+                  if (cc + e < p.N) crow[cc + e] = __float2bfloat16_rn(src[e]);
+              }
+            }
+          }
+        }
+      }
+      // All TMEM reads of this accumulator are complete (waited in tmem_load32).
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    // Give any copy or MMA still in flight time to land before the shared
+    // memory and tensor memory are released (bounded: ~200 us).
+    for (int i = 0; i < 200; ++i) __nanosleep(1000);
+  }
+  tc_fence_after_sync();
+  if (warp == 2) tmem_dealloc<1>(tmem_base, Cfg::kTmemCols);
+}
+
+}  // namespace wst

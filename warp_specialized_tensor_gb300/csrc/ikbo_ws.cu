@@ -1,0 +1,94 @@
+// ikbo_ws.cu -- launcher of the IKBO linear-compression kernel.
+#include "ikbo_ws.cuh"
+#include "wst_host.h"
+
+namespace wst {
+
+int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
+  DeviceInfo dev;
+  int st = current_device_info(&dev);
+  if (st) return st;
+
+  const int F = pr.Du + pr.Dc;
+  IkboArgs a{};
+  a.num_users = pr.num_users;
+  a.num_cand = pr.num_cand;
+  a.Du = pr.Du;
+  a.Dc = pr.Dc;
+  a.D = pr.D;
+  a.O = pr.O;
+  a.kb_u = (pr.Du + 63) / 64;
+  a.kb_c = (pr.Dc + 63) / 64;
+  const size_t w_bytes = align_up((size_t)(a.kb_u + a.kb_c) * pr.O * 128, 1024);
+  const size_t fixed = w_bytes + 1024 /*barriers, flags*/ + 1024 /*alignment slack*/;
+  const size_t smem_cap = dev.max_smem_optin > 0 ? (size_t)dev.max_smem_optin : 232448;
+  if (fixed + 4 * (size_t)kIkboABytes > smem_cap) {
+    set_error("ikbo: W tile of %zu bytes leaves too little shared memory for the ring", w_bytes);
+    return ST_UNSUPPORTED;
+  }
+  int stages = (int)((smem_cap - fixed) / kIkboABytes);
+  if (stages > kIkboMaxStages) stages = kIkboMaxStages;
+  a.stages = stages;
+  a.slots = 512 / pr.O < kIkboMaxSlots ? 512 / pr.O : kIkboMaxSlots;
+  a.uoff = pr.uoff;
+  a.Y = static_cast<float*>(pr.Y);
+  uint8_t* ws = static_cast<uint8_t*>(pr.ws);
+  a.flags = reinterpret_cast<uint32_t*>(ws + ikbo_flags_offset());
+  a.P = reinterpret_cast<float*>(ws + ikbo_partials_offset(pr.num_users));
+  a.ws = reinterpret_cast<WsHeader*>(ws);
+  a.timeout_ns = wait_timeout_ns();
+  // Bytes moved per item: its K-blocks of features plus its fp32 output tile.
+  a.cost_user = (long long)a.kb_u * kIkboABytes + (long long)pr.O * pr.D * 4;
+  a.cost_cand = (long long)a.kb_c * kIkboABytes + (long long)pr.O * pr.D * 4;
+
+  CUtensorMap tmU, tmC, tmW;
+  {
+    uint64_t dims[3] = {(uint64_t)pr.D, (uint64_t)pr.Du, (uint64_t)pr.num_users};
+    uint64_t str[2] = {(uint64_t)pr.D * 2, (uint64_t)pr.Du * pr.D * 2};
+    uint32_t box[3] = {64, 64, 1};
+    if ((st = encode_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pr.U, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    uint64_t dims[3] = {(uint64_t)pr.D, (uint64_t)pr.Dc, (uint64_t)pr.num_cand};
+    uint64_t str[2] = {(uint64_t)pr.D * 2, (uint64_t)pr.Dc * pr.D * 2};
+    uint32_t box[3] = {64, 64, 1};
+    if ((st = encode_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pr.Cf, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    uint64_t dims[2] = {(uint64_t)F, (uint64_t)pr.O};
+    uint64_t str[1] = {(uint64_t)F * 2};
+    uint32_t box[2] = {64, (uint32_t)pr.O};
+    if ((st = encode_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.W, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+
+  const size_t smem = fixed + (size_t)stages * kIkboABytes;
+  cudaError_t e = cudaFuncSetAttribute(k_ikbo_ws, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ikbo)");
+  int grid = dev.num_sms;
+  const long long items = (long long)pr.num_users + pr.num_cand;
+  if (items < grid) grid = (int)items;
+  if (grid < 1) grid = 1;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kIkboThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_ikbo_ws, tmU, tmC, tmW, a);
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_ikbo_ws");
+  return ST_OK;
+}
+
+}  // namespace wst

@@ -1,0 +1,328 @@
+// ikbo_ws.cuh -- in-kernel-broadcast (IKBO) linear compression for sm_103a.
+//
+//   Y[c] = W . concat(U[user(c)], Cf[c])
+//        = W_u . U[user(c)]  +  W_c . Cf[c]          (matmul decomposition)
+//
+// "How We Built TLX: A Hardware-Native GPU Compiler for Production ML at
+// Scale" (Meta Engineering), "Case Study 2: In-Kernel Broadcast Optimization
+// for RecSys" and "TLX Provides a Building Block for the Final Stage of This
+// Optimization": the user features are never replicated per candidate; the
+// user partial product P[u] = W_u . U[u] is computed once per user, and one
+// persistent warp-specialized kernel runs the user GEMMs and the candidate
+// GEMMs through the same shared-memory ring and mbarriers without draining
+// it in between; tile-level release/acquire flags hand P[u] from the CTA
+// that computed it to the CTAs whose candidates need it.
+//
+// GEMM orientation on the tensor core (D = 128 lanes):
+//   user item u : P[u]^T [D x O] = U[u]^T [D x Du] . W_u^T [Du x O]
+//   cand item c : Y[c]^T [D x O] = Cf[c]^T [D x Dc] . W_c^T [Dc x O]  (+ P[u]^T)
+// A = U[u]^T / Cf[c]^T is read straight from the [f][d] layout as an
+// MN-major operand (d contiguous); B = W^T is K-major (W rows are f-contiguous)
+// and stays resident in shared memory for the whole kernel.  TMEM lane d of
+// the accumulator holds the O outputs of embedding position d, so the
+// epilogue writes Y[c][o][d] with d across the warp: fully coalesced.
+//
+// Work per CTA (cooperative launch, every CTA resident): first the user items
+// u = blockIdx.x, blockIdx.x + gridDim.x, ...; then one contiguous range of
+// candidates, sized so that every CTA moves about the same number of bytes.
+// A CTA only ever waits for flags set by the FIRST items of other CTAs, which
+// never wait themselves, so the schedule cannot deadlock; every wait is
+// bounded regardless.
+#pragma once
+
+#include "wst_common.cuh"
+
+namespace wst {
+
+constexpr int kIkboMaxStages = 12;
+constexpr int kIkboMaxSlots = 16;
+constexpr int kIkboThreads = 256;  // warps 0-3 roles, 4-7 epilogue
+constexpr int kIkboABytes = 128 * 64 * 2;  // one K-block of U^T / Cf^T: 64 f x 128 d
+
+struct IkboArgs {
+  int num_users, num_cand, Du, Dc, D, O;
+  int kb_u, kb_c;      // K-blocks of the user and the candidate part
+  int stages, slots;   // ring depth, TMEM accumulator slots
+  const int* uoff;     // device int32[num_users+1]
+  float* Y;
+  uint32_t* flags;     // [num_users]
+  float* P;            // [num_users][O][D]
+  WsHeader* ws;
+  unsigned long long timeout_ns;
+  long long cost_user, cost_cand;  // bytes moved per user / candidate item
+};
+
+// Candidate range [lo, hi) of CTA i: equal byte budgets after the CTA's user items.
+__device__ __forceinline__ int ikbo_cand_boundary(const IkboArgs& p, int i, int grid) {
+  if (i >= grid) return p.num_cand;
+  const long long total = (long long)p.num_users * p.cost_user + (long long)p.num_cand * p.cost_cand;
+  int best = 0;
+  for (int j = 1; j <= i; ++j) {
+    const long long users_before =
+        (long long)(p.num_users / grid) * j + min(j, p.num_users % grid);
+    long long budget = (long long)j * (total / grid) - users_before * p.cost_user;
+    long long b = budget > 0 ? budget / p.cost_cand : 0;
+    if (b > p.num_cand) b = p.num_cand;
+    if ((int)b > best) best = (int)b;
+  }
+  return best;
+}
+
+static __device__ __noinline__ void ikbo_check_offsets(const IkboArgs& p) {
+  bool bad = __ldg(p.uoff) != 0 || __ldg(p.uoff + p.num_users) != p.num_cand;
+  int prev = 0;
+  for (int u = 0; u <= p.num_users && !bad; ++u) {
+    int v = __ldg(p.uoff + u);
+    if (v < prev || v > p.num_cand) bad = true;
+    prev = v;
+  }
+  if (bad) latch_error(p.ws, kErrBadOffsets, 1);
+}
+
+__global__ void __launch_bounds__(kIkboThreads, 1)
+    k_ikbo_ws(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
+              const __grid_constant__ CUtensorMap tmW, const IkboArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int kb_w = p.kb_u + p.kb_c;
+  const int w_kb_bytes = p.O * 128;  // one K-block of W^T: O rows x 128 B
+  uint8_t* smW = smem;
+  uint8_t* smA = smW + align_up((size_t)kb_w * w_kb_bytes, 1024);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smA + (size_t)p.stages * kIkboABytes);
+  // bars: full[stages] | empty[stages] | accf[slots] | acce[slots] | w
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
+  uint32_t* tmem_slot = misc;                       // [0]
+  volatile uint32_t* abort_flag = misc + 1;         // [1]
+  uint32_t* epoch_s = misc + 2;                     // [2]
+  uint32_t* cnt = misc + 4;                         // [4 .. 4+slots): user-publish counters
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t bar_base = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (kIkboMaxStages + s); };
+  auto accf_bar = [&](int a) { return bar_base + 8u * (2 * kIkboMaxStages + a); };
+  auto acce_bar = [&](int a) { return bar_base + 8u * (2 * kIkboMaxStages + kIkboMaxSlots + a); };
+  const uint32_t w_bar = bar_base + 8u * (2 * kIkboMaxStages + 2 * kIkboMaxSlots);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < p.slots; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 4);
+      cnt[a] = 0;
+    }
+    mbar_init(w_bar, 1);
+    *abort_flag = 0u;
+    *epoch_s = p.ws->epoch + 1u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmU);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 2) {
+    tmem_alloc<1>(smem_addr(tmem_slot), 512);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t target = *epoch_s;
+  const Guard guard{p.ws, abort_flag, p.timeout_ns};
+  const int c_lo = ikbo_cand_boundary(p, blockIdx.x, gridDim.x);
+  const int c_hi = ikbo_cand_boundary(p, blockIdx.x + 1, gridDim.x);
+  const int n_user_items =
+      blockIdx.x < (unsigned)p.num_users ? (p.num_users - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int n_items = n_user_items + (c_hi - c_lo);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      if (blockIdx.x == 0) ikbo_check_offsets(p);
+      // W^T, resident for the whole kernel.
+      mbar_arrive_expect_tx(w_bar, (uint32_t)(kb_w * w_kb_bytes));
+      for (int j = 0; j < kb_w; ++j) {
+        const int x = j < p.kb_u ? j * 64 : p.Du + (j - p.kb_u) * 64;
+        tma_load_2d(smem_addr(smW + j * w_kb_bytes), &tmW, w_bar, x, 0);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = 0; it < n_items && ok; ++it) {
+        const bool is_user = it < n_user_items;
+        const int idx = is_user ? (int)blockIdx.x + it * (int)gridDim.x : c_lo + (it - n_user_items);
+        const int nkb = is_user ? p.kb_u : p.kb_c;
+        const CUtensorMap* m = is_user ? &tmU : &tmC;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), kIkboABytes);
+          const uint32_t dA = smem_addr(smA + stage * kIkboABytes);
+          tma_load_3d(dA, m, full_bar(stage), 0, kb * 64, idx);
+          tma_load_3d(dA + kIkboABytes / 2, m, full_bar(stage), 64, kb * 64, idx);
+          if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int i = 0; i < p.stages && ok; ++i) {
+        ok = wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | 0x100 | stage);
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, p.O, /*A MN-major*/ true, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int slot = 0;
+      uint32_t slot_phase = 0;
+      bool ok = wait_phase(guard, w_bar, 0, (kRoleMma << 16) | 0x200);
+      if (ok) tc_fence_after_sync();
+      for (int it = 0; it < n_items && ok; ++it) {
+        const bool is_user = it < n_user_items;
+        const int nkb = is_user ? p.kb_u : p.kb_c;
+        const int wkb0 = is_user ? 0 : p.kb_u;
+        if (!wait_phase(guard, acce_bar(slot), slot_phase ^ 1u, (kRoleMma << 16) | 0x100 | slot)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(slot * p.O);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(guard, full_bar(stage), phase, (kRoleMma << 16) | stage)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t aBase = smem_addr(smA + stage * kIkboABytes);
+          const uint32_t bBase = smem_addr(smW + (wkb0 + kb) * w_kb_bytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // A (MN-major): 16 f-rows of 128 B per step; the two 64-d halves
+            // are 8 KB apart (leading offset), 8-row f groups 1 KB apart.
+            const uint64_t ad = sdesc_sw128(aBase + k * 2048, kIkboABytes / 2, 1024);
+            // B (K-major): 16 f = 32 B per step inside the 128-byte swizzle row.
+            const uint64_t bd = sdesc_sw128(bBase + k * 32, 16, 1024);
+            umma_bf16<1>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(slot));
+        if (++slot == p.slots) { slot = 0; slot_phase ^= 1u; }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int d = q * 32 + (int)lane;  // embedding position = TMEM lane
+    const int nchunk = p.O / 32;
+    int slot = 0;
+    uint32_t slot_phase = 0;
+    int cached_user = -1;
+    int ucur = 0;  // user cursor for the candidate range
+    float pc[2][32];
+    if (c_lo < c_hi) {
+      // first user whose range ends after c_lo
+      int lo = 0, hi = p.num_users - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.uoff + mid + 1) <= c_lo) lo = mid + 1; else hi = mid;
+      }
+      ucur = lo;
+    }
+    for (int it = 0; it < n_items; ++it) {
+      const bool is_user = it < n_user_items;
+      const int idx = is_user ? (int)blockIdx.x + it * (int)gridDim.x : c_lo + (it - n_user_items);
+      if (!is_user) {
+        while (ucur < p.num_users - 1 && __ldg(p.uoff + ucur + 1) <= idx) ++ucur;
+        if (ucur != cached_user) {
+          uint32_t ok = 1;
+          if (lane == 0) ok = wait_flag(guard, p.flags + ucur, target, (kRoleFlag << 16) | (ucur & 0xFFFF)) ? 1u : 0u;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          (void)ld_acquire_gpu(p.flags + ucur);
+          cached_user = ucur;
+          const float* pu = p.P + (size_t)ucur * p.O * p.D;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pc[0][i] = __ldcg(pu + (size_t)i * p.D + d);
+          if (nchunk > 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pc[1][i] = __ldcg(pu + (size_t)(32 + i) * p.D + d);
+          }
+        }
+      }
+      if (!warp_wait_phase(guard, accf_bar(slot), slot_phase, (kRoleEpilogue << 16) | slot)) break;
+      tc_fence_after_sync();
+      const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * p.O);
+      if (is_user) {
+        float* pu = p.P + (size_t)idx * p.O * p.D;
+        for (int j = 0; j < nchunk; ++j) {
+          float v[32];
+          tmem_load32(t_lane + j * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) __stcg(pu + (size_t)(j * 32 + i) * p.D + d, v[i]);
+        }
+        // Publish P[u]: the last of the four epilogue warps to finish its
+        // rows releases flag[u] = this call's epoch.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t old = atomicAdd(cnt + slot, 1u);
+          if ((old & 3u) == 3u) {
+            __threadfence();
+            st_release_gpu(p.flags + idx, target);
+          }
+        }
+      } else {
+        float* yc = p.Y + (size_t)idx * p.O * p.D;
+        const float* pu = p.P + (size_t)ucur * p.O * p.D;
+        for (int j = 0; j < nchunk; ++j) {
+          float v[32];
+          tmem_load32(t_lane + j * 32, v);
+          if (j == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += pc[0][i];
+          } else if (j == 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += pc[1][i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += __ldcg(pu + (size_t)(j * 32 + i) * p.D + d);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) __stcs(yc + (size_t)(j * 32 + i) * p.D + d, v[i]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(slot));
+      if (++slot == p.slots) { slot = 0; slot_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    for (int i = 0; i < 200; ++i) __nanosleep(1000);
+  }
+  tc_fence_after_sync();
+  if (warp == 2) tmem_dealloc<1>(tmem_base, 512);
+  if (threadIdx.x == 0) {
+    // The last CTA to finish advances the workspace epoch for the next call.
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.ws->done_ctas, 1u);
+    if (prev == gridDim.x - 1) {
+      p.ws->done_ctas = 0u;
+      p.ws->epoch = target;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace wst

@@ -1,0 +1,74 @@
+// wst_host.h -- host-side helpers shared by the launchers and the C ABI:
+// tensor-map encoding (driver entry point fetched through the runtime, so
+// the library loads on machines without a driver), device properties, the
+// thread-local error message, and the problem descriptions handed from the
+// validating ABI layer to the per-kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace wst {
+
+// Status codes, identical to wst_status in include/wst.h.
+enum Status : int {
+  ST_OK = 0,
+  ST_INVALID_ARG = 1,
+  ST_ALIGNMENT = 2,
+  ST_UNSUPPORTED = 3,
+  ST_CUDA = 4,
+  ST_TIMEOUT = 5,
+  ST_BAD_OFFSETS = 6,
+};
+
+void set_error(const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);  // records the message, returns ST_CUDA
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;
+};
+int current_device_info(DeviceInfo* out);  // Status
+
+unsigned long long wait_timeout_ns();
+
+// Encode a tiled tensor map (rank 2 or 3).  dims / box innermost first,
+// strides_bytes has rank-1 entries.  Returns Status.
+int encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+               CUtensorMapSwizzle sw);
+
+struct GemmProblem {
+  int grouped;     // 0 dense / batched, 1 grouped
+  int batch;       // dense: batch count; grouped: G
+  int M, N, K;     // grouped: M = M_total
+  const void* A;
+  long long lda, strideA;
+  const void* B;
+  long long ldb, strideB;  // grouped: strideB = per-group stride
+  const void* bias;
+  long long strideBias;
+  void* C;
+  long long ldc, strideC;
+  int c_f32;
+  int epi;
+  const int* offsets;
+  void* ws;
+};
+
+struct IkboProblem {
+  int num_users, num_cand, Du, Dc, D, O;
+  const void* U;
+  const void* Cf;
+  const void* W;
+  const int* uoff;
+  void* Y;
+  void* ws;
+};
+
+int run_gemm(const GemmProblem& p, cudaStream_t stream);
+int run_ikbo(const IkboProblem& p, cudaStream_t stream);
+
+}  // namespace wst
