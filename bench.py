@@ -1,0 +1,496 @@
+"""Benchmark of the hot path: one step = the three contractions once each on
+their full-size synthetic workloads, through the C ABI, on one stream:
+
+  dense     C = A . B^T, M = N = K = 8192, bf16 in, fp32 accumulate, bf16 out
+  grouped   MoE up-projection: 64 experts, 16384 tokens routed top-2,
+            K = 4096, N = 1536 per expert, bf16 out
+  ikbo      linear compression, 64 users x 128 candidates, U[64,256,128],
+            C[8192,64,128], W[32,320], fp32 out
+
+value = algorithmic FLOPs of the step / device time (TFLOP/s), whole job over
+all ranks (each rank runs its own replica: weak scaling).  Inputs are larger
+than L2 (129 MB), so L2 is not flushed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16 TFLOP/s and % of GB300 dense tensor peak (GEMM, grouped, IKBO)"
+UNIT = "TFLOP/s"
+WORKLOAD = ("step = dense GEMM 8192x8192x8192 (bf16 out) + grouped MoE GEMM "
+            "(64 experts, 16384 tokens top-2, K=4096, N=1536, bf16 out) + IKBO linear "
+            "compression (64 users x 128 candidates, Du=256, Dc=64, D=128, O=32, fp32 out)")
+
+# Algorithmic FLOPs (2 per multiply-add) and bytes (each input read once,
+# each output written once) of the three workloads.
+DENSE = dict(M=8192, N=8192, K=8192)
+GROUPED = dict(M=32768, N=1536, K=4096, G=64)
+IKBO = dict(users=64, cand=8192, Du=256, Dc=64, D=128, O=32)
+
+
+def dense_flops(M, N, K, batch=1):
+    return 2.0 * batch * M * N * K
+
+
+def dense_bytes(M, N, K, batch=1, out_bytes=2, shared_b=False):
+    return batch * (M * K * 2 + (0 if shared_b else N * K * 2) + M * N * out_bytes) + \
+        (N * K * 2 if shared_b else 0)
+
+
+def grouped_flops(M, N, K, G):
+    return 2.0 * M * N * K
+
+
+def grouped_bytes(M, N, K, G):
+    return M * K * 2 + G * N * K * 2 + M * N * 2 + (G + 1) * 4
+
+
+def ikbo_flops(users, cand, Du, Dc, D, O):
+    # decomposed form: once per user for the user part, per candidate for the rest
+    return 2.0 * (users * O * Du * D + cand * O * Dc * D)
+
+
+def ikbo_bytes(users, cand, Du, Dc, D, O):
+    return users * Du * D * 2 + cand * Dc * D * 2 + O * (Du + Dc) * 2 + cand * O * D * 4 + \
+        (users + 1) * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def kernel_source_digest():
+    """Digest of the kernel sources, to tell whether committed ncu counters
+    still describe the kernels being timed."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "warp_specialized_tensor_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel]
+        if e.get("source_digest") != kernel_source_digest():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# clocks sampler
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for t, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((t, float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        inside = rows
+        if self.window:
+            w = [r for r in rows if self.window[0] - 0.05 <= r[0] <= self.window[1] + 0.05]
+            if w:
+                inside = w
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, rank, world, dist):
+    import torch
+    import synthetic
+    import warp_specialized_tensor_gb300 as wst
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wst.load_library()
+    peaks = load_peaks()
+
+    d = synthetic.workload("dense8192")
+    g = synthetic.workload("grouped_moe")
+    k = synthetic.workload("ikbo")
+    host = {"dA": d["A"], "dB": d["B"], "gA": g["A"], "gB": g["B"], "goff": g["offsets"],
+            "kU": k["U"], "kC": k["C"], "kW": k["W"], "koff": k["user_offsets"]}
+    dv = {n: t.to(dev) for n, t in host.items()}
+    dC = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev)
+    gC = torch.empty(GROUPED["M"], GROUPED["N"], dtype=torch.bfloat16, device=dev)
+    kY = torch.empty(IKBO["cand"], IKBO["O"], IKBO["D"], dtype=torch.float32, device=dev)
+    ws = wst.workspace(device=dev)
+    wsk = wst.workspace(IKBO["users"], IKBO["O"], IKBO["D"], device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def k_dense():
+        wst.wst_gemm_bf16(dv["dA"], dv["dB"], dC, workspace=ws, stream=stream)
+
+    def k_grouped():
+        wst.wst_grouped_gemm_bf16(dv["gA"], dv["gB"], dv["goff"], gC, workspace=ws, stream=stream)
+
+    def k_ikbo():
+        wst.wst_ikbo_linear_compress(dv["kU"], dv["kC"], dv["kW"], dv["koff"], kY, wsk,
+                                     stream=stream)
+
+    kernels = [("dense", k_dense), ("grouped", k_grouped), ("ikbo", k_ikbo)]
+    if args.only:
+        kernels = [kv for kv in kernels if kv[0] == args.only]
+    flops = {"dense": dense_flops(**DENSE), "grouped": grouped_flops(**GROUPED),
+             "ikbo": ikbo_flops(**IKBO)}
+    nbytes = {"dense": dense_bytes(**DENSE), "grouped": grouped_bytes(**GROUPED),
+              "ikbo": ikbo_bytes(**IKBO)}
+    step_flops = sum(flops[n] for n, _ in kernels)
+
+    # warm-up
+    for _ in range(args.warmup):
+        for _, fn in kernels:
+            fn()
+    torch.cuda.synchronize(dev)
+    for w_ in (ws, wsk):
+        st = wst.wst_sync_status(w_, stream)
+        if st != 0:
+            raise RuntimeError("device error during warm-up: %s" % wst.wst_status_string(st))
+
+    # timed region: K steps, per-kernel events on the launching stream
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for n, _ in kernels}
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.4)  # let the sampler start before the timed region
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_begin.record(stream)
+    for i in range(args.steps):
+        for n, fn in kernels:
+            a, b = ev[n][i]
+            a.record(stream)
+            fn()
+            b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    sampler.mark(wall0, wall1)
+    time.sleep(0.15)
+    sampler.stop()
+    for w_ in (ws, wsk):
+        st = wst.wst_sync_status(w_, stream)
+        if st != 0:
+            raise RuntimeError("device error in timed region: %s" % wst.wst_status_string(st))
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    per_kernel_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n, _ in kernels}
+
+    if dist is not None:
+        import torch.distributed as tdist
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev if tdist.get_backend() == "nccl" else "cpu")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ms_per_step = elapsed_ms / args.steps
+    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+
+    # ---- e2e: host buffers in pinned memory, copies inside the timed region
+    pinned = {n: t.pin_memory() for n, t in host.items()}
+    out_host = {"dC": torch.empty(dC.shape, dtype=dC.dtype).pin_memory(),
+                "gC": torch.empty(gC.shape, dtype=gC.dtype).pin_memory(),
+                "kY": torch.empty(kY.shape, dtype=kY.dtype).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    e2e_steps = max(3, min(args.steps, 20)) if not args.no_e2e else 0
+
+    def e2e_step():
+        for n, t in pinned.items():
+            dv[n].copy_(t, non_blocking=True)
+        for _, fn in kernels:
+            fn()
+        out_host["dC"].copy_(dC, non_blocking=True)
+        out_host["gC"].copy_(gC, non_blocking=True)
+        out_host["kY"].copy_(kY, non_blocking=True)
+
+    e2e_ms = float("nan")
+    if e2e_steps:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        import torch.distributed as tdist
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev if tdist.get_backend() == "nccl" else "cpu")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = step_flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12 if e2e_steps else None
+
+    # ---- context: cuBLAS through torch.matmul on the dense workload (not the product)
+    ctx = {}
+    if not args.no_context:
+        Bt = dv["dB"].t()
+        for _ in range(3):
+            torch.matmul(dv["dA"], Bt)
+        torch.cuda.synchronize(dev)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(10):
+            torch.matmul(dv["dA"], Bt)
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        ctx["torch_matmul_dense_tflops"] = round(flops["dense"] * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e12, 1)
+
+    variants = {}
+    for n, _ in kernels:
+        ms = per_kernel_ms[n]
+        tf = flops[n] / (ms * 1e-3) / 1e12
+        gbs = nbytes[n] / (ms * 1e-3) / 1e9
+        t_flop = flops[n] / (peaks["bf16_tflops"] * 1e12)
+        t_byte = nbytes[n] / (peaks["hbm_gbs"] * 1e9)
+        variants[n] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                       "frac_dense_peak": round(tf / peaks["bf16_tflops"], 4),
+                       "gbs": round(gbs, 1),
+                       "bound": "tensor" if t_flop >= t_byte else "hbm",
+                       "frac_roofline": round(max(t_flop, t_byte) / (ms * 1e-3), 4),
+                       "algorithmic_flops": flops[n], "algorithmic_bytes": nbytes[n]}
+
+    dom = "dense" if "dense" in per_kernel_ms else kernels[0][0]
+    ach = flops[dom] / (per_kernel_ms[dom] * 1e-3) / 1e12
+    roofline = {"kernel": "k_gemm_ws (dense 8192^3)", "bound": "tensor", "achieved": round(ach, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16_tflops"], 4),
+                "traffic": committed_traffic(dom),
+                "peak_source": peaks["source"] + " (burst bf16, cuBLAS)"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, shapes and distributions of the named workloads)",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": len(kernels) * args.steps,
+        "clocks": sampler.summary(),
+        "variants": variants,
+        "peaks": peaks,
+        "context": ctx,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(d, g, k, budget_s=args.cpu_seconds)
+    return result
+
+
+# ----------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# ----------------------------------------------------------------------------
+def oracle_sample(d, g, k, scale: int):
+    """One bounded sample of the step for the fp64 oracle: `scale` rows of the
+    dense GEMM, `scale` rows of one expert, 4*`scale` IKBO candidates.
+    Returns (flops done, seconds)."""
+    import oracle
+    t0 = time.time()
+    rows = list(range(0, 8192, max(1, 8192 // scale)))[:scale]
+    oracle.gemm(d["A"], d["B"], rows=rows)
+    off = g["offsets"].tolist()
+    e = 7
+    r0, r1 = off[e], off[e + 1]
+    sel = list(range(r0, min(r1, r0 + scale)))
+    oracle.gemm(g["A"][sel], g["B"][e])
+    cands = list(range(0, 8192, max(1, 8192 // (4 * scale))))[:4 * scale]
+    oracle.ikbo(k["U"], k["C"], k["W"], k["user_offsets"], cands=cands)
+    dt = time.time() - t0
+    F = IKBO["Du"] + IKBO["Dc"]
+    fl = 2.0 * len(rows) * 8192 * 8192 + 2.0 * len(sel) * 1536 * 4096 + \
+        2.0 * len(cands) * IKBO["O"] * F * IKBO["D"]
+    return fl, dt
+
+
+def cpu_baseline(d, g, k, budget_s: float = 15.0):
+    import oracle
+    fl1, dt1 = oracle_sample(d, g, k, 2)  # calibration
+    rate = fl1 / max(dt1, 1e-6)
+    scale = max(2, int(budget_s * rate / (fl1 / 2) / 1.0))
+    scale = min(scale, 4096)
+    fl, dt = oracle_sample(d, g, k, scale)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d dense rows (all 8192 columns), %d rows of expert 7, %d IKBO candidates; "
+                      "fp64 accumulation, %.1f s" % (scale, scale, 4 * scale, dt)}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    import synthetic
+    oracle.build()
+    d = synthetic.workload("dense8192")
+    g = synthetic.workload("grouped_moe")
+    k = synthetic.workload("ikbo")
+    fl1, dt1 = oracle_sample(d, g, k, 1)
+    per_unit = dt1
+    budget = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
+    scale = max(1, int(budget / max(per_unit, 1e-6)))
+    for _ in range(args.warmup):
+        oracle_sample(d, g, k, scale)
+    tot_fl, tot_dt = 0.0, 0.0
+    for _ in range(args.steps):
+        fl, dt = oracle_sample(d, g, k, scale)
+        tot_fl += fl
+        tot_dt += dt
+    value = tot_fl / tot_dt / 1e12
+    sample = ("per step: %d dense rows (all columns), %d rows of expert 7, %d IKBO candidates "
+              "of the same workload; fp64 oracle on host cores" % (scale, scale, 4 * scale))
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "n/a (CPU)",
+                                        "parallelism": "single process"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["dense", "grouped", "ikbo"], default=None,
+                    help="time one kernel only (profiling runs); not a bench line")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)))
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend)
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(res))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

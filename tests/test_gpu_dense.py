@@ -72,6 +72,23 @@ def test_dense_padded_leading_dims(wst):
     assert torch.isnan(Cb[:, N:].float()).all(), "padding columns were written"
 
 
+def test_dense_k_tail_with_nan_padding(wst):
+    # K = 100 is not a multiple of 8: the rows are padded to 104 elements and
+    # the padding holds NaN, which must never enter the sums.
+    M, N, K, ld = 200, 136, 100, 104
+    d = synthetic.dense(M, N, K, seed=12)
+    Ab = torch.full((M, ld), float("nan"), dtype=torch.bfloat16)
+    Ab[:, :K] = d["A"]
+    Bb = torch.full((N, ld), float("nan"), dtype=torch.bfloat16)
+    Bb[:, :K] = d["B"]
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ws = wst.workspace()
+    wst.wst_gemm_bf16(Ab.cuda()[:, :K], Bb.cuda()[:, :K], C, workspace=ws)
+    assert wst.wst_sync_status(ws) == 0
+    ref = oracle.gemm(d["A"], d["B"])
+    assert_parity(C, ref, K, amax(d["A"]), amax(d["B"]), False, what="K tail")
+
+
 @pytest.mark.parametrize("epi", ["bias", "bias_silu"])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
 def test_batched_epilogues(wst, epi, out):

@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 
       const int row_base = tl.m0 + q * 32;  // first row this warp drains
       const int row = row_base + (int)lane;
-      const bool full_rows = !GROUPED || (row_base + 32 <= tl.row_end);
+      const bool full_rows = row_base + 32 <= tl.row_end;
       const __nv_bfloat16* bias_row =
           EPI ? p.bias + (long long)tl.b * p.bias_stride : nullptr;
       const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -371,10 +371,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         }
         // Chunks that start past the last row / column store nothing (a TMA
         // store is never issued at an out-of-range start coordinate).
+        // A TMA store clips the innermost dimension only at 16-byte
+        // granularity, so chunks that cross the last column (or the last
+        // row of a group) use masked direct stores instead.
         const bool chunk_live = row_base < tl.row_end && tl.n0 + c0 < p.N;
         if (!chunk_live) {
           // nothing to store
-        } else if (full_rows) {
+        } else if (full_rows && tl.n0 + c0 + Cfg::kColsPerChunk <= p.N) {
           // Stage the 32 x 128 B block (128-byte swizzle) and TMA-store it.
           uint8_t* sb = stg + buf * Cfg::kStgBytes;
           if (Cfg::kStageBufs == 2) {
@@ -413,8 +416,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
           }
           if (Cfg::kStageBufs == 2) buf ^= 1;
         } else if (row < tl.row_end) {
-          // Partial group tile: rows past the group end belong to the next
-          // group and must not be written.  Masked direct stores.
+          // Partial tile: rows past the end (for a group: the next group's
+          // rows) and columns past N must not be written.  Masked stores.
           const int colg = tl.n0 + c0;
           if constexpr (OUT_F32) {
             float* crow = reinterpret_cast<float*>(p.C) + (long long)row * p.ldc;
