@@ -195,15 +195,22 @@ def run_ours(args, rank, world, dist):
     wst.load_library()
     peaks = load_peaks()
 
-    d = synthetic.workload("dense8192")
-    g = synthetic.workload("grouped_moe")
-    k = synthetic.workload("ikbo")
-    host = {"dA": d["A"], "dB": d["B"], "gA": g["A"], "gB": g["B"], "goff": g["offsets"],
-            "kU": k["U"], "kC": k["C"], "kW": k["W"], "koff": k["user_offsets"]}
+    need = (args.only,) if args.only else ("dense", "grouped", "ikbo")
+    host = {}
+    d = g = k = None
+    if "dense" in need:
+        d = synthetic.workload("dense8192")
+        host.update({"dA": d["A"], "dB": d["B"]})
+    if "grouped" in need:
+        g = synthetic.workload("grouped_moe")
+        host.update({"gA": g["A"], "gB": g["B"], "goff": g["offsets"]})
+    if "ikbo" in need:
+        k = synthetic.workload("ikbo")
+        host.update({"kU": k["U"], "kC": k["C"], "kW": k["W"], "koff": k["user_offsets"]})
     dv = {n: t.to(dev) for n, t in host.items()}
-    dC = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev)
-    gC = torch.empty(GROUPED["M"], GROUPED["N"], dtype=torch.bfloat16, device=dev)
-    kY = torch.empty(IKBO["cand"], IKBO["O"], IKBO["D"], dtype=torch.float32, device=dev)
+    dC = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev) if d else None
+    gC = torch.empty(GROUPED["M"], GROUPED["N"], dtype=torch.bfloat16, device=dev) if g else None
+    kY = torch.empty(IKBO["cand"], IKBO["O"], IKBO["D"], dtype=torch.float32, device=dev) if k else None
     ws = wst.workspace(device=dev)
     wsk = wst.workspace(IKBO["users"], IKBO["O"], IKBO["D"], device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -282,9 +289,9 @@ def run_ours(args, rank, world, dist):
 
     # ---- e2e: host buffers in pinned memory, copies inside the timed region
     pinned = {n: t.pin_memory() for n, t in host.items()}
-    out_host = {"dC": torch.empty(dC.shape, dtype=dC.dtype).pin_memory(),
-                "gC": torch.empty(gC.shape, dtype=gC.dtype).pin_memory(),
-                "kY": torch.empty(kY.shape, dtype=kY.dtype).pin_memory()}
+    outs = {"dC": dC, "gC": gC, "kY": kY}
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for n, t in outs.items() if t is not None}
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
     e2e_steps = max(3, min(args.steps, 20)) if not args.no_e2e else 0
@@ -294,9 +301,8 @@ def run_ours(args, rank, world, dist):
             dv[n].copy_(t, non_blocking=True)
         for _, fn in kernels:
             fn()
-        out_host["dC"].copy_(dC, non_blocking=True)
-        out_host["gC"].copy_(gC, non_blocking=True)
-        out_host["kY"].copy_(kY, non_blocking=True)
+        for n, t in out_host.items():
+            t.copy_(outs[n], non_blocking=True)
 
     e2e_ms = float("nan")
     if e2e_steps:
@@ -322,7 +328,7 @@ def run_ours(args, rank, world, dist):
 
     # ---- context: cuBLAS through torch.matmul on the dense workload (not the product)
     ctx = {}
-    if not args.no_context:
+    if not args.no_context and d is not None:
         Bt = dv["dB"].t()
         for _ in range(3):
             torch.matmul(dv["dA"], Bt)
@@ -374,7 +380,7 @@ def run_ours(args, rank, world, dist):
         "peaks": peaks,
         "context": ctx,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.only:
         result["cpu_baseline"] = cpu_baseline(d, g, k, budget_s=args.cpu_seconds)
     return result
 
@@ -405,15 +411,57 @@ def oracle_sample(d, g, k, scale: int):
 
 
 def cpu_baseline(d, g, k, budget_s: float = 15.0):
+    """Time the oracle, as it stands, on repeated bounded samples of the step
+    until about budget_s seconds of CPU work are done."""
     import oracle
-    fl1, dt1 = oracle_sample(d, g, k, 2)  # calibration
-    rate = fl1 / max(dt1, 1e-6)
-    scale = max(2, int(budget_s * rate / (fl1 / 2) / 1.0))
-    scale = min(scale, 4096)
-    fl, dt = oracle_sample(d, g, k, scale)
-    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d dense rows (all 8192 columns), %d rows of expert 7, %d IKBO candidates; "
-                      "fp64 accumulation, %.1f s" % (scale, scale, 4 * scale, dt)}
+    scale = 64
+    tot_fl, tot_dt, reps = 0.0, 0.0, 0
+    while tot_dt < budget_s and reps < 1000:
+        fl, dt = oracle_sample(d, g, k, scale)
+        tot_fl += fl
+        tot_dt += dt
+        reps += 1
+    return {"value": tot_fl / tot_dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d x (%d dense rows with all 8192 columns, %d rows of expert 7, %d IKBO "
+                      "candidates); fp64 accumulation; %.1f s" % (reps, scale, scale, 4 * scale, tot_dt)}
+
+
+def record_traffic(report: str, kernel_key: str, regex: str):
+    """Write profiles/traffic.json[kernel_key] from an ncu report of one launch:
+    dram__bytes_read.sum + dram__bytes_write.sum, stamped with the current
+    kernel-source digest (so bench.py reports null once the kernels change)."""
+    import csv
+    import io
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True,
+                         text=True, check=True).stdout
+    rows = list(csv.reader(io.StringIO(out)))
+    hdr, units = rows[0], rows[1]
+    import re
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    launches = []
+    for r in rows[2:]:
+        name = r[hdr.index("Kernel Name")]
+        if not re.search(regex, name):
+            continue
+        tot = 0.0
+        for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            i = hdr.index(m)
+            tot += float(r[i]) * scale[units[i]]
+        launches.append(tot)
+    if not launches:
+        raise SystemExit("no launch of %r in %s" % (regex, report))
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        data = json.load(open(path))
+    except Exception:
+        data = {}
+    data[kernel_key] = {"dram_bytes_per_launch": sum(launches) / len(launches),
+                        "launches": len(launches), "report": os.path.basename(report),
+                        "source_digest": kernel_source_digest()}
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+    print(json.dumps(data[kernel_key]))
 
 
 def run_reference(args, rank, world):

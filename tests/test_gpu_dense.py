@@ -136,3 +136,28 @@ def test_repeated_calls_same_workspace(wst):
     for _ in range(3):
         C = dense_run(wst, d["A"], d["B"], torch.float32, ws=ws)
         assert_parity(C, ref, 128, amax(d["A"]), amax(d["B"]), False, what="repeat")
+
+
+def test_dense_single_cta_path_forced(tmp_path):
+    # The 1-CTA tile path for shapes that would otherwise use CTA pairs
+    # (WST_CTA_GROUP is read once per process, hence a child process).
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = r'''
+import sys, torch
+sys.path.insert(0, %r); sys.path.insert(0, %r)
+import oracle, synthetic
+import warp_specialized_tensor_gb300 as wst
+from gpu_util import amax, assert_parity, dense_run
+d = synthetic.dense(300, 264, 200, batch=3, seed=31, bias=True)
+C = dense_run(wst, d["A"], d["B"], torch.bfloat16, bias=d["bias"], epi="bias_silu")
+ref = oracle.gemm(d["A"], d["B"], bias=d["bias"], epi="bias_silu")
+assert_parity(C, ref, 200, amax(d["A"]), amax(d["B"]), True, what="1-CTA forced")
+print("ok")
+''' % (root, os.path.join(root, "tests"))
+    env = dict(os.environ, WST_CTA_GROUP="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr

@@ -10,7 +10,8 @@ int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   DeviceInfo dev;
   int st = current_device_info(&dev);
   if (st) return st;
-  return pr.grouped ? run_gemm_grouped(pr, dev, stream) : dispatch<false>(pr, dev, stream);
+  return pr.grouped ? run_gemm_grouped(pr, dev, stream) : (dense_cta_group(pr.M) == 2 ? dispatch<false, 2>(pr, dev, stream)
+                                              : dispatch<false, 1>(pr, dev, stream));
 }
 
 }  // namespace wst

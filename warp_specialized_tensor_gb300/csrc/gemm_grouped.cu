@@ -5,7 +5,7 @@
 namespace wst {
 
 int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
-  return dispatch<true>(pr, dev, stream);
+  return dispatch<true, 1>(pr, dev, stream);
 }
 
 }  // namespace wst

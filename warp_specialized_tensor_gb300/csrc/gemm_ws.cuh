@@ -43,8 +43,9 @@ struct GemmArgs {
   int a3d, b3d, c3d;      // operand maps carry a batch / group coordinate
   const __nv_bfloat16* bias;
   long long bias_stride;
-  void* C;                // for masked stores of partial group tiles
+  void* C;                // for masked stores of partial tiles
   long long ldc;
+  long long c_stride;     // batch stride of C in elements (dense batched)
   const int* offsets;     // grouped: device int32[G+1]
   int G, M_total;
   WsHeader* ws;
@@ -61,7 +62,7 @@ struct Tile {
 // --------------------------------------------------------------------------
 // schedulers
 // --------------------------------------------------------------------------
-template <int BN>
+template <int BN, int TM>
 __device__ __forceinline__ Tile dense_tile(const GemmArgs& p, long long t) {
   const long long per_batch = (long long)p.m_tiles * p.n_tiles;
   const int b = (int)(t / per_batch);
@@ -75,7 +76,7 @@ __device__ __forceinline__ Tile dense_tile(const GemmArgs& p, long long t) {
   const int rr = r - bi * band;
   const int m = first_m + rr % rows;
   const int n = rr / rows;
-  return Tile{b, m * kBM, n * BN, p.M};
+  return Tile{b, m * TM, n * BN, p.M};
 }
 
 // Walks the groups in order; every role of a CTA runs its own walker over
@@ -176,12 +177,15 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED>
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED, int CG>
 struct GemmCfg {
   static constexpr int kThreads = 128 + 32 * EPI_WARPS;
-  static constexpr int kABytes = kBM * kBK * 2;        // 16 KB
-  static constexpr int kBBytes = BN * kBK * 2;         // 32 KB at BN = 256
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTileM = kBM * CG;              // rows of one (cluster) tile
+  static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows
+  static constexpr int kBRows = BN / CG;               // this CTA's share of the B tile
+  static constexpr int kBBytes = kBRows * kBK * 2;     // 32 KB (1-CTA) / 16 KB (pair)
+  static constexpr int kStageBytes = kABytes + kBBytes;  // per CTA
+  static constexpr uint32_t kTxBytes = CG * kStageBytes;  // expected by the leader's full[s]
   static constexpr int kStageBufs = EPI_WARPS == 4 ? 2 : 1;  // staging buffers per epilogue warp
   static constexpr int kStgBytes = 32 * 128;           // 32 rows x 128 B
   static constexpr int kColsPerChunk = OUT_F32 ? 32 : 64;
@@ -193,13 +197,20 @@ struct GemmCfg {
   static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kWarpCols % kColsPerChunk == 0, "epilogue chunking");
+  static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
 };
 
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED>
+// CG = 2: a cluster of two CTAs computes one 256 x BN tile with
+// tcgen05.mma.cta_group::2 issued by the even CTA (the leader).  Each CTA
+// loads its own 128 rows of A and its half of B's BN rows (no multicast);
+// both CTAs' loads complete on the leader's full[s]; the leader's commits
+// arrive on empty[s] / acc_full[a] in both CTAs; both epilogues arrive on the
+// leader's acc_empty[a]; each CTA drains its own 128 accumulator rows.
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED, int CG>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     k_gemm_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
-  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, GROUPED>;
+  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, GROUPED, CG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -218,6 +229,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
   auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;   // CTA rank in the pair
+  const long long cluster_id = blockIdx.x / CG;
+  const long long num_clusters = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), EPI_WARPS);
+      mbar_init(acce_bar(a), CG * EPI_WARPS);
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -235,11 +249,12 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     tma_prefetch_desc(&tmC);
   }
   if (warp == 2) {
-    tmem_alloc<1>(smem_addr(tmem_slot), Cfg::kTmemCols);
-    tmem_relinquish<1>();
+    tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const Guard guard{p.ws, abort_flag, p.timeout_ns};
@@ -253,41 +268,59 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
       bool ok = true;
       GroupWalker gw;
       if (GROUPED) gw.init(p, p.n_tiles);
-      for (long long t = blockIdx.x; ok; t += gridDim.x) {
+      for (long long t = cluster_id; ok; t += num_clusters) {
         Tile tl;
         if constexpr (GROUPED) {
           if (!gw.seek(p, p.n_tiles, t)) break;
           tl = gw.tile<BN>(t);
         } else {
           if (t >= p.tiles_total) break;
-          tl = dense_tile<BN>(p, t);
+          tl = dense_tile<BN, Cfg::kTileM>(p, t);
         }
+        const int a_row = tl.m0 + (int)rank * kBM;
+        const int b_row = tl.n0 + (int)rank * Cfg::kBRows;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
+          const bool got = CG == 2
+              ? wait_phase_cluster(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)
+              : wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage);
+          if (!got) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+          // The leader's full[s] expects both CTAs' bytes; the peer only
+          // contributes its copies' completions.
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::kTxBytes);
           const uint32_t dA = smem_addr(smA + stage * Cfg::kABytes);
           const uint32_t dB = smem_addr(smB + stage * Cfg::kBBytes);
           const int kx = kb * kBK;
-          if (p.a3d) tma_load_3d(dA, &tmA, full_bar(stage), kx, tl.m0, tl.b);
-          else       tma_load_2d(dA, &tmA, full_bar(stage), kx, tl.m0);
-          if (p.b3d) tma_load_3d(dB, &tmB, full_bar(stage), kx, tl.n0, tl.b);
-          else       tma_load_2d(dB, &tmB, full_bar(stage), kx, tl.n0);
+          if constexpr (CG == 1) {
+            if (p.a3d) tma_load_3d(dA, &tmA, full_bar(stage), kx, a_row, tl.b);
+            else       tma_load_2d(dA, &tmA, full_bar(stage), kx, a_row);
+            if (p.b3d) tma_load_3d(dB, &tmB, full_bar(stage), kx, b_row, tl.b);
+            else       tma_load_2d(dB, &tmB, full_bar(stage), kx, b_row);
+          } else {
+            const uint32_t fb = map_to_cta(full_bar(stage), 0);
+            if (p.a3d) tma_load_3d_pair(dA, &tmA, fb, kx, a_row, tl.b);
+            else       tma_load_2d_pair(dA, &tmA, fb, kx, a_row);
+            if (p.b3d) tma_load_3d_pair(dB, &tmB, fb, kx, b_row, tl.b);
+            else       tma_load_2d_pair(dB, &tmB, fb, kx, b_row);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       // Drain: every slot released => every MMA that read the ring completed.
       for (int i = 0; i < STAGES && ok; ++i) {
-        ok = wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | 0x100 | stage);
+        ok = CG == 2
+            ? wait_phase_cluster(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | 0x100 | stage)
+            : wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | 0x100 | stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, false);
+    // Only the leader CTA of a pair issues MMAs (for both CTAs).
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(Cfg::kTileM, BN, false, false);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -295,13 +328,16 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
       bool ok = true;
       GroupWalker gw;
       if (GROUPED) gw.init(p, p.n_tiles);
-      for (long long t = blockIdx.x; ok; t += gridDim.x) {
+      for (long long t = cluster_id; ok; t += num_clusters) {
         if constexpr (GROUPED) {
           if (!gw.seek(p, p.n_tiles, t)) break;
         } else {
           if (t >= p.tiles_total) break;
         }
-        if (!wait_phase(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc)) break;
+        const bool free_acc = CG == 2
+            ? wait_phase_cluster(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc)
+            : wait_phase(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc);
+        if (!free_acc) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -316,13 +352,17 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t ad = sdesc_sw128(aBase + k * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(bBase + k * 32, 16, 1024);
-            umma_bf16<1>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(empty_bar(stage));  // slot free once these MMAs finish
+          // slot free (in both CTAs) once these MMAs finish
+          if constexpr (CG == 1) umma_commit(empty_bar(stage));
+          else                   umma_commit_pair(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(accf_bar(acc));  // accumulator complete
+        // accumulator complete (in both CTAs)
+        if constexpr (CG == 1) umma_commit(accf_bar(acc));
+        else                   umma_commit_pair(accf_bar(acc), 0x3);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
     }
@@ -337,19 +377,23 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     int buf = 0;
     GroupWalker gw;
     if (GROUPED) gw.init(p, p.n_tiles);
-    for (long long t = blockIdx.x;; t += gridDim.x) {
+    for (long long t = cluster_id;; t += num_clusters) {
       Tile tl;
       if constexpr (GROUPED) {
         if (!gw.seek(p, p.n_tiles, t)) break;
         tl = gw.tile<BN>(t);
       } else {
         if (t >= p.tiles_total) break;
-        tl = dense_tile<BN>(p, t);
+        tl = dense_tile<BN, Cfg::kTileM>(p, t);
       }
-      if (!warp_wait_phase(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc)) break;
+      const bool got = CG == 2
+          ? warp_wait_phase_cluster(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc)
+          : warp_wait_phase(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc);
+      if (!got) break;
       tc_fence_after_sync();
 
-      const int row_base = tl.m0 + q * 32;  // first row this warp drains
+      // first row this warp drains (this CTA holds rows rank*128 .. +127 of the tile)
+      const int row_base = tl.m0 + (int)rank * kBM + q * 32;
       const int row = row_base + (int)lane;
       const bool full_rows = row_base + 32 <= tl.row_end;
       const __nv_bfloat16* bias_row =
@@ -419,8 +463,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
           // Partial tile: rows past the end (for a group: the next group's
           // rows) and columns past N must not be written.  Masked stores.
           const int colg = tl.n0 + c0;
+          // Dense: tl.b is the batch entry; grouped: rows are absolute (stride 0).
+          const long long row_off = (GROUPED ? 0ll : (long long)tl.b * p.c_stride) +
+                                    (long long)row * p.ldc;
           if constexpr (OUT_F32) {
-            float* crow = reinterpret_cast<float*>(p.C) + (long long)row * p.ldc;
+            float* crow = reinterpret_cast<float*>(p.C) + row_off;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int cc = colg + 4 * j;
@@ -433,7 +480,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
               }
             }
           } else {
-            __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc;
+            __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(p.C) + row_off;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int cc = colg + 8 * j;
@@ -456,7 +503,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
       // All TMEM reads of this accumulator are complete (waited in tmem_load32).
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (lane == 0) {
+        if constexpr (CG == 1) mbar_arrive(acce_bar(acc));
+        else                   mbar_arrive_cluster(map_to_cta(acce_bar(acc), 0));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -470,8 +520,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     // memory and tensor memory are released (bounded: ~200 us).
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
   }
+  // No CTA of a pair leaves while its peer may still arrive on its barriers.
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after_sync();
-  if (warp == 2) tmem_dealloc<1>(tmem_base, Cfg::kTmemCols);
+  if (warp == 2) tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
 }
 
 }  // namespace wst

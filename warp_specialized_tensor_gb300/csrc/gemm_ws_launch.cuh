@@ -2,6 +2,8 @@
 // tensor maps, kernel arguments, grid size, launch.  Included by the two
 // translation units that instantiate the dense and the grouped variants.
 #pragma once
+#include <cstdlib>
+
 #include "gemm_ws.cuh"
 #include "wst_host.h"
 
@@ -10,13 +12,28 @@ namespace wst {
 namespace {
 
 constexpr int kBN = 256;
-constexpr int kStages = 4;
 
-template <bool OUT_F32, int EPI, bool GROUPED>
+// Ring depth: 4 x 48 KB (1-CTA tile) or 6 x 32 KB per CTA (2-CTA pair).
+template <int CG>
+constexpr int stages_for() { return CG == 2 ? 6 : 4; }
+
+// CTA-pair tiles for dense problems with more than one 128-row block, unless
+// WST_CTA_GROUP=1|2 forces a choice (tuning runs).
+inline int dense_cta_group(int M) {
+  static int forced = [] {
+    const char* s = std::getenv("WST_CTA_GROUP");
+    return s ? std::atoi(s) : 0;
+  }();
+  if (forced == 1 || forced == 2) return forced;
+  return M > kBM ? 2 : 1;
+}
+
+template <bool OUT_F32, int EPI, bool GROUPED, int CG>
 int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
   constexpr int EW = EPI == 2 ? 8 : 4;
-  using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, GROUPED>;
-  auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, GROUPED>;
+  constexpr int kStages = stages_for<CG>();
+  using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, GROUPED, CG>;
+  auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, GROUPED, CG>;
 
   // ---- tensor maps
   CUtensorMap tmA, tmB, tmC;
@@ -41,7 +58,7 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
     {
       uint64_t dims[3] = {(uint64_t)pr.K, (uint64_t)pr.N, (uint64_t)pr.batch};
       uint64_t str[2] = {(uint64_t)pr.ldb * 2, (uint64_t)pr.strideB * 2};
-      uint32_t box[3] = {64, (uint32_t)kBN, 1};
+      uint32_t box[3] = {64, (uint32_t)Cfg::kBRows, 1};
       if ((st = encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.b3d ? 3 : 2, pr.B, dims, str,
                            box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
@@ -69,7 +86,7 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
     {
       uint64_t dims[3] = {(uint64_t)pr.K, (uint64_t)pr.N, (uint64_t)pr.batch};
       uint64_t str[2] = {(uint64_t)pr.ldb * 2, (uint64_t)pr.strideB * 2};
-      uint32_t box[3] = {64, (uint32_t)kBN, 1};
+      uint32_t box[3] = {64, (uint32_t)Cfg::kBRows, 1};
       if ((st = encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.b3d ? 3 : 2, pr.B, dims, str,
                            box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
@@ -88,7 +105,7 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   a.M = pr.M;
   a.N = pr.N;
   a.K = pr.K;
-  a.m_tiles = (pr.M + kBM - 1) / kBM;
+  a.m_tiles = (pr.M + Cfg::kTileM - 1) / Cfg::kTileM;
   a.n_tiles = (pr.N + kBN - 1) / kBN;
   a.k_blocks = (pr.K + kBK - 1) / kBK;
   a.tiles_total = GROUPED ? 0 : (long long)pr.batch * a.m_tiles * a.n_tiles;
@@ -97,15 +114,45 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   a.bias_stride = pr.strideBias;
   a.C = pr.C;
   a.ldc = pr.ldc;
+  a.c_stride = GROUPED ? 0 : pr.strideC;
   a.offsets = pr.offsets;
   a.G = GROUPED ? pr.batch : 0;
   a.M_total = pr.M;
   a.ws = static_cast<WsHeader*>(pr.ws);
   a.timeout_ns = wait_timeout_ns();
 
+  // Persistent grid: one CTA (pair) per SM (pair) that can be resident.
   long long grid = dev.num_sms;
-  if (!GROUPED && a.tiles_total < grid) grid = a.tiles_total;
-  if (grid < 1) grid = 1;
+  if (CG == 2) {
+    static int max_clusters[64] = {0};
+    int& mc = max_clusters[dev.device & 63];
+    if (mc == 0) {
+      cudaLaunchConfig_t q{};
+      q.gridDim = dim3((unsigned)(dev.num_sms & ~1), 1, 1);
+      q.blockDim = dim3(Cfg::kThreads, 1, 1);
+      q.dynamicSmemBytes = Cfg::kSmemBytes;
+      cudaLaunchAttribute ca[1];
+      ca[0].id = cudaLaunchAttributeClusterDimension;
+      ca[0].val.clusterDim.x = 2;
+      ca[0].val.clusterDim.y = 1;
+      ca[0].val.clusterDim.z = 1;
+      q.attrs = ca;
+      q.numAttrs = 1;
+      cudaError_t qe = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)Cfg::kSmemBytes);
+      if (qe != cudaSuccess) return cuda_fail(qe, "cudaFuncSetAttribute(gemm)");
+      int n = 0;
+      qe = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+      if (qe != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = dev.num_sms / 2;
+      }
+      mc = n;
+    }
+    grid = 2ll * mc;
+  }
+  if (!GROUPED && a.tiles_total * CG < grid) grid = a.tiles_total * CG;
+  if (grid < CG) grid = CG;
 
   // ---- launch
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -116,26 +163,31 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG == 2 ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
   if (e != cudaSuccess) return cuda_fail(e, "launch k_gemm_ws");
   return ST_OK;
 }
 
-template <bool GROUPED>
+template <bool GROUPED, int CG>
 int dispatch(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t s) {
   if (pr.c_f32) {
     switch (pr.epi) {
-      case 0: return launch_cfg<true, 0, GROUPED>(pr, dev, s);
-      case 1: return launch_cfg<true, 1, GROUPED>(pr, dev, s);
-      default: return launch_cfg<true, 2, GROUPED>(pr, dev, s);
+      case 0: return launch_cfg<true, 0, GROUPED, CG>(pr, dev, s);
+      case 1: return launch_cfg<true, 1, GROUPED, CG>(pr, dev, s);
+      default: return launch_cfg<true, 2, GROUPED, CG>(pr, dev, s);
     }
   }
   switch (pr.epi) {
-    case 0: return launch_cfg<false, 0, GROUPED>(pr, dev, s);
-    case 1: return launch_cfg<false, 1, GROUPED>(pr, dev, s);
-    default: return launch_cfg<false, 2, GROUPED>(pr, dev, s);
+    case 0: return launch_cfg<false, 0, GROUPED, CG>(pr, dev, s);
+    case 1: return launch_cfg<false, 1, GROUPED, CG>(pr, dev, s);
+    default: return launch_cfg<false, 2, GROUPED, CG>(pr, dev, s);
   }
 }
 

@@ -95,6 +95,14 @@ __device__ __forceinline__ bool warp_wait_phase(const Guard& g, uint32_t bar, ui
   return ok != 0;
 }
 
+__device__ __forceinline__ bool warp_wait_phase_cluster(const Guard& g, uint32_t bar,
+                                                        uint32_t parity, uint32_t info) {
+  uint32_t ok = 0;
+  if (lane_id() == 0) ok = wait_phase_cluster(g, bar, parity, info) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
 // Bounded spin until *flag == want (acquire, gpu scope).
 static __device__ __noinline__ bool wait_flag(const Guard& g, const uint32_t* flag, uint32_t want,
                                        uint32_t info) {
