@@ -86,27 +86,35 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def kernel_source_digest():
-    """Digest of the kernel sources, to tell whether committed ncu counters
-    still describe the kernels being timed."""
+KERNEL_SOURCES = {
+    "dense": ["sm103.cuh", "wst_common.cuh", "gemm_ws.cuh", "gemm_ws_launch.cuh", "gemm_dense.cu"],
+    "grouped": ["sm103.cuh", "wst_common.cuh", "grouped_ws.cuh", "grouped_ws.cu"],
+    "ikbo": ["sm103.cuh", "wst_common.cuh", "ikbo_ws.cuh", "ikbo_ws.cu"],
+}
+
+
+def kernel_source_digest(kernel: str):
+    """Digest of one kernel's sources, to tell whether committed ncu counters
+    still describe the kernel being timed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "warp_specialized_tensor_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
+    for f in KERNEL_SOURCES[kernel]:
+        path = os.path.join(csrc, f)
+        if os.path.exists(path):
+            with open(path, "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None if the
-    kernel sources changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         e = t[kernel]
-        if e.get("source_digest") != kernel_source_digest():
+        if e.get("source_digest") != kernel_source_digest(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -458,7 +466,7 @@ def record_traffic(report: str, kernel_key: str, regex: str):
         data = {}
     data[kernel_key] = {"dram_bytes_per_launch": sum(launches) / len(launches),
                         "launches": len(launches), "report": os.path.basename(report),
-                        "source_digest": kernel_source_digest()}
+                        "source_digest": kernel_source_digest(kernel_key)}
     with open(path, "w") as f:
         json.dump(data, f, indent=1, sort_keys=True)
     print(json.dumps(data[kernel_key]))
@@ -510,7 +518,12 @@ def main():
                     help="time one kernel only (profiling runs); not a bench line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KEY", "REGEX"),
+                    help="store DRAM bytes per launch from an ncu report in profiles/traffic.json")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(*args.record_traffic)
+        return 0
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 
