@@ -1,0 +1,99 @@
+// grouped_ws.cu -- instantiations and launcher of the grouped (MoE) GEMM.
+#include "grouped_ws.cuh"
+#include "wst_host.h"
+
+namespace wst {
+
+namespace {
+
+template <bool OUT_F32, int EPI>
+int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
+  auto kern = k_grouped_ws<OUT_F32, EPI>;
+  int st;
+  CUtensorMap tmW, tmX;
+  GroupedArgs a{};
+  a.w_shared = (pr.strideB == 0) ? 1 : 0;
+  {
+    // B[g] rows (expert output features), K contiguous: {K, N, G}
+    uint64_t dims[3] = {(uint64_t)pr.K, (uint64_t)pr.N, (uint64_t)(a.w_shared ? 1 : pr.batch)};
+    uint64_t str[2] = {(uint64_t)pr.ldb * 2,
+                       (uint64_t)(a.w_shared ? (long long)pr.N * pr.ldb : pr.strideB) * 2};
+    uint32_t box[3] = {64, 128, 1};
+    if ((st = encode_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pr.B, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    // token rows of A, K contiguous: {K, M_total}
+    uint64_t dims[2] = {(uint64_t)pr.K, (uint64_t)pr.M};
+    uint64_t str[1] = {(uint64_t)pr.lda * 2};
+    uint32_t box[2] = {64, 128};
+    if ((st = encode_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.A, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  a.G = pr.batch;
+  a.M_total = pr.M;
+  a.N = pr.N;
+  a.K = pr.K;
+  a.n_tiles = (pr.N + kGrpTileN - 1) / kGrpTileN;
+  a.k_blocks = (pr.K + kGrpBK - 1) / kGrpBK;
+  a.offsets = pr.offsets;
+  a.bias = static_cast<const __nv_bfloat16*>(pr.bias);
+  a.bias_stride = pr.strideBias;
+  a.C = pr.C;
+  a.ldc = pr.ldc;
+  a.ws = static_cast<WsHeader*>(pr.ws);
+  a.timeout_ns = wait_timeout_ns();
+
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kGrpSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped)");
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kGrpThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGrpSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent grid: every CTA pair that can be resident at once.
+  static int max_clusters[64] = {0};
+  int& mc = max_clusters[dev.device & 63];
+  if (mc == 0) {
+    cfg.gridDim = dim3((unsigned)(dev.num_sms & ~1), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = dev.num_sms / 2;
+    }
+    mc = n;
+  }
+  cfg.gridDim = dim3((unsigned)(2 * mc), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a);
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_grouped_ws");
+  return ST_OK;
+}
+
+}  // namespace
+
+int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
+  if (pr.c_f32) {
+    switch (pr.epi) {
+      case 0: return launch_grouped<true, 0>(pr, dev, stream);
+      case 1: return launch_grouped<true, 1>(pr, dev, stream);
+      default: return launch_grouped<true, 2>(pr, dev, stream);
+    }
+  }
+  switch (pr.epi) {
+    case 0: return launch_grouped<false, 0>(pr, dev, stream);
+    case 1: return launch_grouped<false, 1>(pr, dev, stream);
+    default: return launch_grouped<false, 2>(pr, dev, stream);
+  }
+}
+
+}  // namespace wst

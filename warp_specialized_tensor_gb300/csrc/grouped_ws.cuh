@@ -1,0 +1,352 @@
+// grouped_ws.cuh -- persistent, warp-specialized grouped GEMM (mixture-of-
+// experts expert matmuls) for sm_103a, on CTA pairs.
+//
+// Group g owns token rows [off[g], off[g+1]) of A and C and the weight matrix
+// B[g] (N x K, K contiguous):   C[t][n] = sum_k A[t][k] * B[g][n][k].
+//
+// The tensor core computes the transposed tile  D[n][t] = B[g][n][:] . A[t][:]
+// ("swap AB"): the expert's output features n sit on the 256-row MMA side
+// (two CTAs x 128 TMEM lanes), and the tokens of the group sit on the MMA's N
+// side, whose size is a multiple of 16 up to 256.  A group of T tokens is cut
+// into ceil(T/256) token tiles whose last one is only rounded up to 16, so a
+// ragged group wastes at most 15 token columns instead of up to 127 rows of a
+// 128-row tile.  Both operands are K-major in memory, as the hardware wants.
+//
+// Roles per CTA (persistent, one CTA per SM, pairs in clusters of 2):
+//   warp 0     TMA producer: this CTA's 128 rows of B[g] and its half of the
+//              token tile (rows t0 + rank*Ntile/2 ...) per 64-wide K-block;
+//              both CTAs' copies complete on the leader's full[s].
+//   warp 1     MMA issuer (leader CTA only): tcgen05.mma.cta_group::2,
+//              M = 256, N = token-tile width, into one of two TMEM
+//              accumulators; commits release ring slots / accumulators in
+//              both CTAs.
+//   warp 2     TMEM allocation (both CTAs, 512 columns).
+//   warps 4-7  epilogue: each warp drains its 32 feature lanes, 32 tokens at a
+//              time, adds bias / SiLU, transposes through a private shared
+//              buffer and writes whole 64-byte (bf16) / 128-byte (fp32) row
+//              segments of C with masked vector stores, so rows past the
+//              group end (the next expert's tokens) are never touched.
+//
+// "How We Built TLX: A Hardware-Native GPU Compiler for Production ML at
+// Scale" (Meta Engineering): "TLX in Production" and "Case Study 3:
+// Distributed Grouped GEMM for LLM Pretraining" (grouped expert GEMM),
+// "Introducing TLX" (producer / MMA / epilogue roles over an mbarrier ring).
+#pragma once
+
+#include "wst_common.cuh"
+
+namespace wst {
+
+constexpr int kGrpTileN = 256;   // feature rows per CTA pair (MMA M)
+constexpr int kGrpTileT = 256;   // tokens per tile (MMA N, last tile of a group narrower)
+constexpr int kGrpBK = 64;
+constexpr int kGrpStages = 6;
+constexpr int kGrpEpiWarps = 4;
+constexpr int kGrpThreads = 128 + 32 * kGrpEpiWarps;
+constexpr int kGrpWBytes = 128 * kGrpBK * 2;   // this CTA's 128 rows of B[g]
+constexpr int kGrpXBytes = 128 * kGrpBK * 2;   // up to 128 token rows (box height)
+constexpr int kGrpStageBytes = kGrpWBytes + kGrpXBytes;
+constexpr int kGrpStgBytes = 32 * 32 * 4;      // per-warp transpose buffer (fp32 worst case)
+constexpr size_t kGrpSmemBytes = (size_t)kGrpStages * kGrpStageBytes +
+                                 (size_t)kGrpEpiWarps * kGrpStgBytes + 256 + 1024;
+static_assert(kGrpSmemBytes <= 232448, "shared memory per CTA");
+
+struct GroupedArgs {
+  int G, M_total, N, K;
+  int n_tiles, k_blocks;
+  const int* offsets;  // device int32[G+1]
+  const __nv_bfloat16* bias;
+  long long bias_stride;
+  void* C;
+  long long ldc;
+  int w_shared;        // 1: every group uses the same weight matrix (group stride 0)
+  WsHeader* ws;
+  unsigned long long timeout_ns;
+};
+
+struct GrpTile {
+  int g;      // group
+  int t0;     // first token row (absolute)
+  int nt;     // valid tokens in this tile (1..256)
+  int nmma;   // MMA N: nt rounded up to 16
+  int n0;     // first feature row of B[g] / column of C
+};
+
+// Walks groups in order; every role of a CTA runs its own walker over the
+// same increasing tile indices.  Offsets are clamped into [0, M_total].
+struct GrpWalker {
+  int g;
+  long long base, count;
+  int r0, r1, tt;
+
+  __device__ __forceinline__ void load(const GroupedArgs& p) {
+    if (g >= p.G) { count = 0; return; }
+    int a = __ldg(p.offsets + g);
+    int b = __ldg(p.offsets + g + 1);
+    a = min(max(a, 0), p.M_total);
+    b = min(max(b, a), p.M_total);
+    r0 = a;
+    r1 = b;
+    tt = (b - a + kGrpTileT - 1) / kGrpTileT;
+    count = (long long)tt * p.n_tiles;
+  }
+  __device__ __forceinline__ void init(const GroupedArgs& p) {
+    g = 0;
+    base = 0;
+    load(p);
+  }
+  __device__ __forceinline__ bool seek(const GroupedArgs& p, long long t) {
+    while (g < p.G && t >= base + count) {
+      base += count;
+      ++g;
+      load(p);
+    }
+    return g < p.G;
+  }
+  // n-tile fastest: consecutive tiles share the token block (L2 reuse).
+  __device__ __forceinline__ GrpTile tile(const GroupedArgs& p, long long t) const {
+    const int r = (int)(t - base);
+    const int tok = r / p.n_tiles;
+    const int nt_i = r - tok * p.n_tiles;
+    GrpTile x;
+    x.g = g;
+    x.t0 = r0 + tok * kGrpTileT;
+    x.nt = min(kGrpTileT, r1 - x.t0);
+    x.nmma = (x.nt + 15) & ~15;
+    x.n0 = nt_i * kGrpTileN;
+    return x;
+  }
+};
+
+static __device__ __noinline__ void grouped_check_offsets(const GroupedArgs& p) {
+  bool bad = __ldg(p.offsets) != 0 || __ldg(p.offsets + p.G) != p.M_total;
+  int prev = 0;
+  for (int g = 0; g <= p.G && !bad; ++g) {
+    const int v = __ldg(p.offsets + g);
+    if (v < prev || v > p.M_total) bad = true;
+    prev = v;
+  }
+  if (bad) latch_error(p.ws, kErrBadOffsets, 2);
+}
+
+__device__ __forceinline__ float grp_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+template <bool OUT_F32, int EPI>
+__global__ void __launch_bounds__(kGrpThreads, 1)
+    k_grouped_ws(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const GroupedArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smW = smem;
+  uint8_t* smX = smW + kGrpStages * kGrpWBytes;
+  uint8_t* smStg = smX + kGrpStages * kGrpXBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smStg + kGrpEpiWarps * kGrpStgBytes);
+  // bars: full[S] | empty[S] | acc_full[2] | acc_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 4);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t bar_base = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (kGrpStages + s); };
+  auto accf_bar = [&](int a) { return bar_base + 8u * (2 * kGrpStages + a); };
+  auto acce_bar = [&](int a) { return bar_base + 8u * (2 * kGrpStages + 2 + a); };
+  const uint32_t rank = cluster_ctarank();
+  const long long cluster_id = blockIdx.x / 2;
+  const long long num_clusters = gridDim.x / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGrpStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 2 * kGrpEpiWarps);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 2) {
+    tmem_alloc<2>(smem_addr(tmem_slot), 512);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const Guard guard{p.ws, abort_flag, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      if (blockIdx.x == 0) grouped_check_offsets(p);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      GrpWalker gw;
+      gw.init(p);
+      for (long long t = cluster_id; ok && gw.seek(p, t); t += num_clusters) {
+        const GrpTile tl = gw.tile(p, t);
+        const int w_row = tl.n0 + (int)rank * 128;
+        const int x_row = tl.t0 + (int)rank * (tl.nmma >> 1);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase_cluster(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * kGrpStageBytes);
+          const uint32_t fb = map_to_cta(full_bar(stage), 0);
+          const int kx = kb * kGrpBK;
+          tma_load_3d_pair(smem_addr(smW + stage * kGrpWBytes), &tmW, fb, kx, w_row,
+                           p.w_shared ? 0 : tl.g);
+          tma_load_2d_pair(smem_addr(smX + stage * kGrpXBytes), &tmX, fb, kx, x_row);
+          if (++stage == kGrpStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int i = 0; i < kGrpStages && ok; ++i) {
+        ok = wait_phase_cluster(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | 0x100 | stage);
+        if (++stage == kGrpStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      GrpWalker gw;
+      gw.init(p);
+      for (long long t = cluster_id; ok && gw.seek(p, t); t += num_clusters) {
+        const GrpTile tl = gw.tile(p, t);
+        const uint32_t idesc = idesc_bf16_f32(kGrpTileN, tl.nmma, false, false);
+        if (!wait_phase_cluster(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kGrpTileT);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase(guard, full_bar(stage), phase, (kRoleMma << 16) | stage)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t wBase = smem_addr(smW + stage * kGrpWBytes);
+          const uint32_t xBase = smem_addr(smX + stage * kGrpXBytes);
+#pragma unroll
+          for (int k = 0; k < kGrpBK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(wBase + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(xBase + k * 32, 16, 1024);
+            umma_bf16<2>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(empty_bar(stage), 0x3);
+          if (++stage == kGrpStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(accf_bar(acc), 0x3);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint8_t* stg = smStg + (warp - 4) * kGrpStgBytes;
+    const uint32_t stg_addr = smem_addr(stg);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    GrpWalker gw;
+    gw.init(p);
+    for (long long t = cluster_id; gw.seek(p, t); t += num_clusters) {
+      const GrpTile tl = gw.tile(p, t);
+      if (!warp_wait_phase_cluster(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc)) break;
+      tc_fence_after_sync();
+      const int n_base = tl.n0 + (int)rank * 128 + q * 32;  // this warp's 32 features
+      const int n_lane = n_base + (int)lane;
+      float bias_v = 0.0f;
+      if constexpr (EPI != 0) {
+        if (n_lane < p.N) bias_v = __bfloat162float(p.bias[(long long)tl.g * p.bias_stride + n_lane]);
+      }
+      const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kGrpTileT);
+#pragma unroll 1
+      for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
+        float v[32];
+        tmem_load32(t_lane + c0, v);
+        if constexpr (EPI != 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] += bias_v;
+            if constexpr (EPI == 2) v[j] = grp_silu(v[j]);
+          }
+        }
+        // Transpose: lane (feature) writes column `lane` of the [token][feature] block.
+        if constexpr (OUT_F32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg_addr + j * 128u + lane * 4u), "f"(v[j]) : "memory");
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg_addr + j * 64u + lane * 2u),
+                         "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
+          }
+        }
+        __syncwarp();
+        // Row segments of C: 64 B (bf16) / 128 B (fp32) per token row.
+        constexpr int kSegs = OUT_F32 ? 8 : 4;        // 16-byte segments per row
+        constexpr int kRowsPerPass = 32 / kSegs;
+        constexpr int kElems = OUT_F32 ? 4 : 8;       // elements per segment
+        const int seg = (int)lane % kSegs;
+        const int ncol = n_base + seg * kElems;
+#pragma unroll
+        for (int pass = 0; pass < kSegs; ++pass) {
+          const int row = (int)lane / kSegs + pass * kRowsPerPass;  // token within the chunk
+          const int tok = c0 + row;
+          const uint32_t src = stg_addr + row * (OUT_F32 ? 128u : 64u) + seg * 16u;
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(src));
+          if (tok < tl.nt && ncol < p.N) {
+            const long long off = (long long)(tl.t0 + tok) * p.ldc + ncol;
+            if (ncol + kElems <= p.N) {
+              if constexpr (OUT_F32) *reinterpret_cast<uint4*>(reinterpret_cast<float*>(p.C) + off) = w;
+              else *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.C) + off) = w;
+            } else {
+              const uint32_t parts[4] = {w.x, w.y, w.z, w.w};
+              for (int e = 0; e < kElems && ncol + e < p.N; ++e) {
+                if constexpr (OUT_F32) {
+                  reinterpret_cast<float*>(p.C)[off + e] = __uint_as_float(parts[e]);
+                } else {
+                  const unsigned short hv = (unsigned short)(parts[e >> 1] >> ((e & 1) * 16));
+                  reinterpret_cast<unsigned short*>(p.C)[off + e] = hv;
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(acc), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    for (int i = 0; i < 200; ++i) __nanosleep(1000);
+  }
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 2) tmem_dealloc<2>(tmem_base, 512);
+}
+
+}  // namespace wst

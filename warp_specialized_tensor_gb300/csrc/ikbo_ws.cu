@@ -20,7 +20,8 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   a.kb_u = (pr.Du + 63) / 64;
   a.kb_c = (pr.Dc + 63) / 64;
   const size_t w_bytes = align_up((size_t)(a.kb_u + a.kb_c) * pr.O * 128, 1024);
-  const size_t fixed = w_bytes + 1024 /*barriers, flags*/ + 1024 /*alignment slack*/;
+  const size_t fixed = w_bytes + 4 * 2 * kIkboStgBytes /*output staging*/ +
+                       1024 /*barriers, flags*/ + 1024 /*alignment slack*/;
   const size_t smem_cap = dev.max_smem_optin > 0 ? (size_t)dev.max_smem_optin : 232448;
   if (fixed + 4 * (size_t)kIkboABytes > smem_cap) {
     set_error("ikbo: W tile of %zu bytes leaves too little shared memory for the ring", w_bytes);
@@ -37,11 +38,8 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   a.P = reinterpret_cast<float*>(ws + ikbo_partials_offset(pr.num_users));
   a.ws = reinterpret_cast<WsHeader*>(ws);
   a.timeout_ns = wait_timeout_ns();
-  // Bytes moved per item: its K-blocks of features plus its fp32 output tile.
-  a.cost_user = (long long)a.kb_u * kIkboABytes + (long long)pr.O * pr.D * 4;
-  a.cost_cand = (long long)a.kb_c * kIkboABytes + (long long)pr.O * pr.D * 4;
 
-  CUtensorMap tmU, tmC, tmW;
+  CUtensorMap tmU, tmC, tmW, tmY;
   {
     uint64_t dims[3] = {(uint64_t)pr.D, (uint64_t)pr.Du, (uint64_t)pr.num_users};
     uint64_t str[2] = {(uint64_t)pr.D * 2, (uint64_t)pr.Du * pr.D * 2};
@@ -67,14 +65,46 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
       return st;
   }
 
+  {
+    // Y viewed as [num_cand * O rows][D] fp32; box = one warp's 32 o x 32 d block.
+    uint64_t dims[2] = {(uint64_t)pr.D, (uint64_t)pr.num_cand * pr.O};
+    uint64_t str[1] = {(uint64_t)pr.D * 4};
+    uint32_t box[2] = {32, 32};
+    if ((st = encode_map(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pr.Y, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return st;
+  }
+
   const size_t smem = fixed + (size_t)stages * kIkboABytes;
   cudaError_t e = cudaFuncSetAttribute(k_ikbo_ws, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ikbo)");
-  int grid = dev.num_sms;
+  int grid = dev.num_sms < kIkboMaxGrid ? dev.num_sms : kIkboMaxGrid;
   const long long items = (long long)pr.num_users + pr.num_cand;
   if (items < grid) grid = (int)items;
   if (grid < 1) grid = 1;
+
+  // Candidate split: CTA i first runs users i, i+grid, ...; then candidates
+  // [split[i], split[i+1]).  Each item costs the bytes it moves (its feature
+  // K-blocks plus its fp32 output tile); ranges are contiguous and balance
+  // the cumulative cost (a running maximum keeps them non-decreasing).
+  {
+    const long long cu = (long long)a.kb_u * kIkboABytes + (long long)pr.O * pr.D * 4;
+    const long long cc = (long long)a.kb_c * kIkboABytes + (long long)pr.O * pr.D * 4;
+    const long long total = (long long)pr.num_users * cu + (long long)pr.num_cand * cc;
+    int best = 0;
+    a.split[0] = 0;
+    for (int j = 1; j < grid; ++j) {
+      const long long users_before =
+          (long long)(pr.num_users / grid) * j + (j < pr.num_users % grid ? j : pr.num_users % grid);
+      const long long budget = total * j / grid - users_before * cu;
+      long long b = budget > 0 ? budget / cc : 0;
+      if (b > pr.num_cand) b = pr.num_cand;
+      if ((int)b > best) best = (int)b;
+      a.split[j] = best;
+    }
+    a.split[grid] = pr.num_cand;
+  }
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -86,7 +116,7 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_ikbo_ws, tmU, tmC, tmW, a);
+  e = cudaLaunchKernelEx(&cfg, k_ikbo_ws, tmU, tmC, tmW, tmY, a);
   if (e != cudaSuccess) return cuda_fail(e, "launch k_ikbo_ws");
   return ST_OK;
 }

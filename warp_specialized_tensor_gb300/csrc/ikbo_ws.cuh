@@ -38,6 +38,8 @@ constexpr int kIkboMaxStages = 12;
 constexpr int kIkboMaxSlots = 16;
 constexpr int kIkboThreads = 256;  // warps 0-3 roles, 4-7 epilogue
 constexpr int kIkboABytes = 128 * 64 * 2;  // one K-block of U^T / Cf^T: 64 f x 128 d
+constexpr int kIkboMaxGrid = 256;          // CTAs (<= SMs) the candidate split covers
+constexpr int kIkboStgBytes = 32 * 32 * 4; // per-warp output staging: 32 o x 32 d fp32
 
 struct IkboArgs {
   int num_users, num_cand, Du, Dc, D, O;
@@ -49,24 +51,10 @@ struct IkboArgs {
   float* P;            // [num_users][O][D]
   WsHeader* ws;
   unsigned long long timeout_ns;
-  long long cost_user, cost_cand;  // bytes moved per user / candidate item
+  // Candidate range of CTA i is [split[i], split[i+1]): contiguous ranges
+  // sized on the host so every CTA moves about the same number of bytes.
+  int split[kIkboMaxGrid + 1];
 };
-
-// Candidate range [lo, hi) of CTA i: equal byte budgets after the CTA's user items.
-__device__ __forceinline__ int ikbo_cand_boundary(const IkboArgs& p, int i, int grid) {
-  if (i >= grid) return p.num_cand;
-  const long long total = (long long)p.num_users * p.cost_user + (long long)p.num_cand * p.cost_cand;
-  int best = 0;
-  for (int j = 1; j <= i; ++j) {
-    const long long users_before =
-        (long long)(p.num_users / grid) * j + min(j, p.num_users % grid);
-    long long budget = (long long)j * (total / grid) - users_before * p.cost_user;
-    long long b = budget > 0 ? budget / p.cost_cand : 0;
-    if (b > p.num_cand) b = p.num_cand;
-    if ((int)b > best) best = (int)b;
-  }
-  return best;
-}
 
 static __device__ __noinline__ void ikbo_check_offsets(const IkboArgs& p) {
   bool bad = __ldg(p.uoff) != 0 || __ldg(p.uoff + p.num_users) != p.num_cand;
@@ -81,7 +69,8 @@ static __device__ __noinline__ void ikbo_check_offsets(const IkboArgs& p) {
 
 __global__ void __launch_bounds__(kIkboThreads, 1)
     k_ikbo_ws(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
-              const __grid_constant__ CUtensorMap tmW, const IkboArgs p) {
+              const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
+              const IkboArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -89,7 +78,8 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   const int w_kb_bytes = p.O * 128;  // one K-block of W^T: O rows x 128 B
   uint8_t* smW = smem;
   uint8_t* smA = smW + align_up((size_t)kb_w * w_kb_bytes, 1024);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smA + (size_t)p.stages * kIkboABytes);
+  uint8_t* smY = smA + (size_t)p.stages * kIkboABytes;  // 4 warps x 2 x 4 KB output staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smY + 4 * 2 * kIkboStgBytes);
   // bars: full[stages] | empty[stages] | accf[slots] | acce[slots] | w
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
   uint32_t* tmem_slot = misc;                       // [0]
@@ -123,6 +113,7 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
     tma_prefetch_desc(&tmU);
     tma_prefetch_desc(&tmC);
     tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmY);
   }
   if (warp == 2) {
     tmem_alloc<1>(smem_addr(tmem_slot), 512);
@@ -134,8 +125,8 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t target = *epoch_s;
   const Guard guard{p.ws, abort_flag, p.timeout_ns};
-  const int c_lo = ikbo_cand_boundary(p, blockIdx.x, gridDim.x);
-  const int c_hi = ikbo_cand_boundary(p, blockIdx.x + 1, gridDim.x);
+  const int c_lo = p.split[blockIdx.x];
+  const int c_hi = p.split[blockIdx.x + 1];
   const int n_user_items =
       blockIdx.x < (unsigned)p.num_users ? (p.num_users - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int n_items = n_user_items + (c_hi - c_lo);
@@ -225,6 +216,7 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
     int slot = 0;
     uint32_t slot_phase = 0;
     int cached_user = -1;
+    int ybuf = 0;
     int ucur = 0;  // user cursor for the candidate range
     float pc[2][32];
     if (c_lo < c_hi) {
@@ -280,7 +272,6 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
           }
         }
       } else {
-        float* yc = p.Y + (size_t)idx * p.O * p.D;
         const float* pu = p.P + (size_t)ucur * p.O * p.D;
         for (int j = 0; j < nchunk; ++j) {
           float v[32];
@@ -295,8 +286,22 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] += __ldcg(pu + (size_t)(j * 32 + i) * p.D + d);
           }
+          // Stage this warp's 32 o x 32 d block (row o = 128 B, lane = d) and
+          // TMA-store it to Y[idx][32j .. 32j+31][32q .. 32q+31].
+          uint8_t* sb = smY + ((q * 2 + ybuf) * kIkboStgBytes);
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          const uint32_t base = smem_addr(sb) + lane * 4u;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) __stcs(yc + (size_t)(j * 32 + i) * p.D + d, v[i]);
+          for (int i = 0; i < 32; ++i)
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + i * 128u), "f"(v[i]) : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, smem_addr(sb), q * 32, idx * p.O + j * 32);
+            bulk_commit_group();
+          }
+          ybuf ^= 1;
         }
       }
       tc_fence_before_sync();
@@ -304,6 +309,8 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
       if (lane == 0) mbar_arrive(acce_bar(slot));
       if (++slot == p.slots) { slot = 0; slot_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
