@@ -87,7 +87,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "dense": ["sm103.cuh", "wst_common.cuh", "gemm_ws.cuh", "gemm_ws_launch.cuh", "gemm_dense.cu"],
+    "dense": ["sm103.cuh", "wst_common.cuh", "gemm_ws.cuh", "gemm_dense.cu"],
     "grouped": ["sm103.cuh", "wst_common.cuh", "grouped_ws.cuh", "grouped_ws.cu"],
     "ikbo": ["sm103.cuh", "wst_common.cuh", "ikbo_ws.cuh", "ikbo_ws.cu"],
 }

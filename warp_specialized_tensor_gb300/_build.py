@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwst.so")
 
 SOURCES = ["gemm_dense.cu", "grouped_ws.cu", "ikbo_ws.cu", "wst_api.cu"]
-HEADERS = ["sm103.cuh", "wst_common.cuh", "gemm_ws.cuh", "gemm_ws_launch.cuh", "grouped_ws.cuh", "ikbo_ws.cuh",
+HEADERS = ["sm103.cuh", "wst_common.cuh", "gemm_ws.cuh", "grouped_ws.cuh", "ikbo_ws.cuh",
            "wst_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

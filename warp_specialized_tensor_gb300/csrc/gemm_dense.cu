@@ -1,8 +1,163 @@
-// gemm_dense.cu -- dense / strided-batched instantiations of the
-// warp-specialized GEMM, and the entry used by the C ABI.
-#include "gemm_ws_launch.cuh"
+// gemm_dense.cu -- instantiations and launcher of the warp-specialized dense /
+// strided-batched GEMM: tensor maps, kernel arguments, grid size, launch.
+#include <cstdlib>
+
+#include "gemm_ws.cuh"
+#include "wst_host.h"
 
 namespace wst {
+
+namespace {
+
+constexpr int kBN = 256;
+
+// Ring depth: 4 x 48 KB (1-CTA tile) or 6 x 32 KB per CTA (2-CTA pair).
+template <int CG>
+constexpr int stages_for() { return CG == 2 ? 6 : 4; }
+
+// CTA-pair tiles for dense problems with more than one 128-row block, unless
+// WST_CTA_GROUP=1|2 forces a choice (tuning runs).
+inline int dense_cta_group(int M) {
+  static int forced = [] {
+    const char* s = std::getenv("WST_CTA_GROUP");
+    return s ? std::atoi(s) : 0;
+  }();
+  if (forced == 1 || forced == 2) return forced;
+  return M > kBM ? 2 : 1;
+}
+
+template <bool OUT_F32, int EPI, int CG>
+int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
+  constexpr int EW = EPI == 2 ? 8 : 4;
+  constexpr int kStages = stages_for<CG>();
+  using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, CG>;
+  auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, CG>;
+
+  // ---- tensor maps
+  CUtensorMap tmA, tmB, tmC;
+  GemmArgs a{};
+  const CUtensorMapDataType out_dt =
+      OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t es = OUT_F32 ? 4 : 2;
+  const uint32_t cw = OUT_F32 ? 32 : 64;
+  int st;
+  a.a3d = (pr.batch > 1 && pr.strideA != 0);
+  a.b3d = (pr.batch > 1 && pr.strideB != 0);
+  a.c3d = (pr.batch > 1);
+  {
+    uint64_t dims[3] = {(uint64_t)pr.K, (uint64_t)pr.M, (uint64_t)pr.batch};
+    uint64_t str[2] = {(uint64_t)pr.lda * 2, (uint64_t)pr.strideA * 2};
+    uint32_t box[3] = {64, 128, 1};
+    if ((st = encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a3d ? 3 : 2, pr.A, dims, str,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    uint64_t dims[3] = {(uint64_t)pr.K, (uint64_t)pr.N, (uint64_t)pr.batch};
+    uint64_t str[2] = {(uint64_t)pr.ldb * 2, (uint64_t)pr.strideB * 2};
+    uint32_t box[3] = {64, (uint32_t)Cfg::kBRows, 1};
+    if ((st = encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.b3d ? 3 : 2, pr.B, dims, str,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    uint64_t dims[3] = {(uint64_t)pr.N, (uint64_t)pr.M, (uint64_t)pr.batch};
+    uint64_t str[2] = {(uint64_t)pr.ldc * es, (uint64_t)pr.strideC * es};
+    uint32_t box[3] = {cw, 32, 1};
+    if ((st = encode_map(&tmC, out_dt, a.c3d ? 3 : 2, pr.C, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+
+  // ---- arguments
+  a.batch = pr.batch;
+  a.M = pr.M;
+  a.N = pr.N;
+  a.K = pr.K;
+  a.m_tiles = (pr.M + Cfg::kTileM - 1) / Cfg::kTileM;
+  a.n_tiles = (pr.N + kBN - 1) / kBN;
+  a.k_blocks = (pr.K + kBK - 1) / kBK;
+  a.tiles_total = (long long)pr.batch * a.m_tiles * a.n_tiles;
+  a.group_m = 16;
+  a.bias = static_cast<const __nv_bfloat16*>(pr.bias);
+  a.bias_stride = pr.strideBias;
+  a.C = pr.C;
+  a.ldc = pr.ldc;
+  a.c_stride = pr.strideC;
+  a.ws = static_cast<WsHeader*>(pr.ws);
+  a.timeout_ns = wait_timeout_ns();
+
+  // Persistent grid: one CTA (pair) per SM (pair) that can be resident.
+  long long grid = dev.num_sms;
+  if (CG == 2) {
+    static int max_clusters[64] = {0};
+    int& mc = max_clusters[dev.device & 63];
+    if (mc == 0) {
+      cudaLaunchConfig_t q{};
+      q.gridDim = dim3((unsigned)(dev.num_sms & ~1), 1, 1);
+      q.blockDim = dim3(Cfg::kThreads, 1, 1);
+      q.dynamicSmemBytes = Cfg::kSmemBytes;
+      cudaLaunchAttribute ca[1];
+      ca[0].id = cudaLaunchAttributeClusterDimension;
+      ca[0].val.clusterDim.x = 2;
+      ca[0].val.clusterDim.y = 1;
+      ca[0].val.clusterDim.z = 1;
+      q.attrs = ca;
+      q.numAttrs = 1;
+      cudaError_t qe = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)Cfg::kSmemBytes);
+      if (qe != cudaSuccess) return cuda_fail(qe, "cudaFuncSetAttribute(gemm)");
+      int n = 0;
+      qe = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+      if (qe != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = dev.num_sms / 2;
+      }
+      mc = n;
+    }
+    grid = 2ll * mc;
+  }
+  if (a.tiles_total * CG < grid) grid = a.tiles_total * CG;
+  if (grid < CG) grid = CG;
+
+  // ---- launch
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Cfg::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG == 2 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_gemm_ws");
+  return ST_OK;
+}
+
+template <int CG>
+int dispatch(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t s) {
+  if (pr.c_f32) {
+    switch (pr.epi) {
+      case 0: return launch_cfg<true, 0, CG>(pr, dev, s);
+      case 1: return launch_cfg<true, 1, CG>(pr, dev, s);
+      default: return launch_cfg<true, 2, CG>(pr, dev, s);
+    }
+  }
+  switch (pr.epi) {
+    case 0: return launch_cfg<false, 0, CG>(pr, dev, s);
+    case 1: return launch_cfg<false, 1, CG>(pr, dev, s);
+    default: return launch_cfg<false, 2, CG>(pr, dev, s);
+  }
+}
+
+}  // namespace
 
 int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream);
 
@@ -10,8 +165,8 @@ int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   DeviceInfo dev;
   int st = current_device_info(&dev);
   if (st) return st;
-  return pr.grouped ? run_gemm_grouped(pr, dev, stream) : (dense_cta_group(pr.M) == 2 ? dispatch<false, 2>(pr, dev, stream)
-                                              : dispatch<false, 1>(pr, dev, stream));
+  if (pr.grouped) return run_gemm_grouped(pr, dev, stream);
+  return dense_cta_group(pr.M) == 2 ? dispatch<2>(pr, dev, stream) : dispatch<1>(pr, dev, stream);
 }
 
 }  // namespace wst

@@ -1,7 +1,7 @@
 // gemm_ws.cuh -- persistent, warp-specialized bf16 GEMM for sm_103a.
 //
-// One kernel template serves the dense / strided-batched GEMM and the
-// grouped (mixture-of-experts) GEMM.  Per CTA (one per SM, persistent):
+// Dense / strided-batched GEMM.  Per CTA (one per SM, persistent; with
+// CG = 2 a cluster of two CTAs shares one 256 x BN tile):
 //
 //   warp 0      TMA producer: one thread streams A and B K-blocks (64 bf16 =
 //               128 B rows, 128-byte swizzle) into a STAGES-deep shared-memory
@@ -23,8 +23,7 @@
 // "Introducing TLX" (producer / MMA / epilogue roles, NUM_STAGES ring with
 // load and dot barriers, TMEM accumulator, use_acc = k > 0), made persistent
 // ("TLX Provides a Building Block ...": one persistent kernel, ping-pong
-// between consumers) and extended to variable-size groups for expert
-// matmuls ("Case Study 3: Distributed Grouped GEMM for LLM Pretraining").
+// between consumers).
 #pragma once
 
 #include "wst_common.cuh"
@@ -38,7 +37,7 @@ constexpr int kUmmaK = 16;   // K per tcgen05.mma (kind::f16)
 struct GemmArgs {
   int batch, M, N, K;
   int m_tiles, n_tiles, k_blocks;
-  long long tiles_total;  // dense only
+  long long tiles_total;
   int group_m;            // raster: m-tiles per band
   int a3d, b3d, c3d;      // operand maps carry a batch / group coordinate
   const __nv_bfloat16* bias;
@@ -46,17 +45,15 @@ struct GemmArgs {
   void* C;                // for masked stores of partial tiles
   long long ldc;
   long long c_stride;     // batch stride of C in elements (dense batched)
-  const int* offsets;     // grouped: device int32[G+1]
-  int G, M_total;
   WsHeader* ws;
   unsigned long long timeout_ns;
 };
 
 struct Tile {
-  int b;        // batch (dense) or group (grouped)
-  int m0;       // first row (absolute row of A / C)
+  int b;        // batch entry
+  int m0;       // first row
   int n0;       // first column
-  int row_end;  // rows >= row_end are not part of this tile's problem
+  int row_end;  // rows >= row_end are outside the problem
 };
 
 // --------------------------------------------------------------------------
@@ -77,62 +74,6 @@ __device__ __forceinline__ Tile dense_tile(const GemmArgs& p, long long t) {
   const int m = first_m + rr % rows;
   const int n = rr / rows;
   return Tile{b, m * TM, n * BN, p.M};
-}
-
-// Walks the groups in order; every role of a CTA runs its own walker over
-// the same increasing tile indices, so they agree on the sequence.
-struct GroupWalker {
-  int g;            // current group
-  long long base;   // first global tile index of group g
-  long long count;  // tiles in group g
-  int row0, row1;   // clamped rows of group g
-  int mt;           // m-tiles of group g
-
-  __device__ __forceinline__ void load(const GemmArgs& p, int n_tiles) {
-    if (g >= p.G) { count = 0; return; }
-    int a = __ldg(p.offsets + g);
-    int b = __ldg(p.offsets + g + 1);
-    a = min(max(a, 0), p.M_total);
-    b = min(max(b, a), p.M_total);
-    row0 = a;
-    row1 = b;
-    mt = (b - a + kBM - 1) / kBM;
-    count = (long long)mt * n_tiles;
-  }
-  __device__ __forceinline__ void init(const GemmArgs& p, int n_tiles) {
-    g = 0;
-    base = 0;
-    load(p, n_tiles);
-  }
-  // Advance to the group holding tile t; false when t is past the last tile.
-  __device__ __forceinline__ bool seek(const GemmArgs& p, int n_tiles, long long t) {
-    while (g < p.G && t >= base + count) {
-      base += count;
-      ++g;
-      load(p, n_tiles);
-    }
-    return g < p.G;
-  }
-  template <int BN>
-  __device__ __forceinline__ Tile tile(long long t) const {
-    const int r = (int)(t - base);
-    const int m = r % mt;  // m-minor: consecutive tiles share the expert's B columns
-    const int n = r / mt;
-    return Tile{g, row0 + m * kBM, n * BN, row1};
-  }
-};
-
-// One pass over all offsets by one thread: latch kErrBadOffsets if they are
-// not non-decreasing from 0 to M_total.
-static __device__ __noinline__ void check_offsets(const GemmArgs& p) {
-  bool bad = __ldg(p.offsets) != 0 || __ldg(p.offsets + p.G) != p.M_total;
-  int prev = 0;
-  for (int g = 0; g <= p.G && !bad; ++g) {
-    int v = __ldg(p.offsets + g);
-    if (v < prev || v > p.M_total) bad = true;
-    prev = v;
-  }
-  if (bad) latch_error(p.ws, kErrBadOffsets, 0);
 }
 
 // --------------------------------------------------------------------------
@@ -177,7 +118,7 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED, int CG>
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG>
 struct GemmCfg {
   static constexpr int kThreads = 128 + 32 * EPI_WARPS;
   static constexpr int kTileM = kBM * CG;              // rows of one (cluster) tile
@@ -206,11 +147,11 @@ struct GemmCfg {
 // both CTAs' loads complete on the leader's full[s]; the leader's commits
 // arrive on empty[s] / acc_full[a] in both CTAs; both epilogues arrive on the
 // leader's acc_empty[a]; each CTA drains its own 128 accumulator rows.
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, bool GROUPED, int CG>
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     k_gemm_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
-  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, GROUPED, CG>;
+  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, CG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,21 +203,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      if (GROUPED && blockIdx.x == 0) check_offsets(p);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      GroupWalker gw;
-      if (GROUPED) gw.init(p, p.n_tiles);
-      for (long long t = cluster_id; ok; t += num_clusters) {
-        Tile tl;
-        if constexpr (GROUPED) {
-          if (!gw.seek(p, p.n_tiles, t)) break;
-          tl = gw.tile<BN>(t);
-        } else {
-          if (t >= p.tiles_total) break;
-          tl = dense_tile<BN, Cfg::kTileM>(p, t);
-        }
+      for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
+        const Tile tl = dense_tile<BN, Cfg::kTileM>(p, t);
         const int a_row = tl.m0 + (int)rank * kBM;
         const int b_row = tl.n0 + (int)rank * Cfg::kBRows;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -326,14 +257,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      GroupWalker gw;
-      if (GROUPED) gw.init(p, p.n_tiles);
-      for (long long t = cluster_id; ok; t += num_clusters) {
-        if constexpr (GROUPED) {
-          if (!gw.seek(p, p.n_tiles, t)) break;
-        } else {
-          if (t >= p.tiles_total) break;
-        }
+      for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
         const bool free_acc = CG == 2
             ? wait_phase_cluster(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc)
             : wait_phase(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc);
@@ -375,17 +299,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int buf = 0;
-    GroupWalker gw;
-    if (GROUPED) gw.init(p, p.n_tiles);
-    for (long long t = cluster_id;; t += num_clusters) {
-      Tile tl;
-      if constexpr (GROUPED) {
-        if (!gw.seek(p, p.n_tiles, t)) break;
-        tl = gw.tile<BN>(t);
-      } else {
-        if (t >= p.tiles_total) break;
-        tl = dense_tile<BN, Cfg::kTileM>(p, t);
-      }
+    for (long long t = cluster_id; t < p.tiles_total; t += num_clusters) {
+      const Tile tl = dense_tile<BN, Cfg::kTileM>(p, t);
       const bool got = CG == 2
           ? warp_wait_phase_cluster(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc)
           : warp_wait_phase(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc);
@@ -417,7 +332,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         // store is never issued at an out-of-range start coordinate).
         // A TMA store clips the innermost dimension only at 16-byte
         // granularity, so chunks that cross the last column (or the last
-        // row of a group) use masked direct stores instead.
+        // row) use masked direct stores instead.
         const bool chunk_live = row_base < tl.row_end && tl.n0 + c0 < p.N;
         if (!chunk_live) {
           // nothing to store
@@ -460,12 +375,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
           }
           if (Cfg::kStageBufs == 2) buf ^= 1;
         } else if (row < tl.row_end) {
-          // Partial tile: rows past the end (for a group: the next group's
-          // rows) and columns past N must not be written.  Masked stores.
+          // Partial tile: rows past M and columns past N must not be
+          // written.  Masked stores.
           const int colg = tl.n0 + c0;
-          // Dense: tl.b is the batch entry; grouped: rows are absolute (stride 0).
-          const long long row_off = (GROUPED ? 0ll : (long long)tl.b * p.c_stride) +
-                                    (long long)row * p.ldc;
+          const long long row_off = (long long)tl.b * p.c_stride + (long long)row * p.ldc;
           if constexpr (OUT_F32) {
             float* crow = reinterpret_cast<float*>(p.C) + row_off;
 #pragma unroll
