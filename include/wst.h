@@ -36,8 +36,9 @@
  * --------------------------------
  *  - All matrix pointers are DEVICE pointers to memory the caller owns and
  *    keeps alive until the work on `stream` has finished.  The library never
- *    allocates, frees or keeps device memory of its own, and never falls back
- *    to the CPU.
+ *    allocates or frees device memory and never falls back to the CPU; the
+ *    only device memory it keeps is the fixed scratch array of
+ *    wst_ikbo_linear_compress_noalloc.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call is asynchronous: it validates its arguments on the host, enqueues
  *    one kernel on `stream`, and returns.
@@ -154,6 +155,36 @@ wst_status wst_ikbo_linear_compress(int num_users, int num_cand, int Du, int Dc,
                                     const void* U, const void* Cf, const void* W,
                                     const int* d_user_offsets,
                                     void* Y, void* workspace, void* stream);
+
+/*
+ * Allocation-free form of wst_ikbo_linear_compress (the pages have no
+ * counterpart; this is a library convenience).  For callers that cannot
+ * allocate device memory when they call -- code under a fixed memory budget,
+ * behind an allocator it must not bypass, or inside a host framework that
+ * owns every allocation -- the per-user partial products, ready flags and
+ * error word live in a device array inside the library instead of a
+ * caller-owned workspace.  Same arguments and results as
+ * wst_ikbo_linear_compress, minus the workspace, plus:
+ *   d_status  optional DEVICE int32 (NULL to skip) that receives this call's
+ *             device-side status (0, WST_ERR_TIMEOUT or WST_ERR_BAD_OFFSETS)
+ *             once the call's work on `stream` has run.
+ * Limits and behaviour:
+ *  - The array holds 4 MiB on every GPU that loads the library, until the
+ *    process exits; wst_workspace_size(num_users, O, D) must not exceed it
+ *    (64 users at O = 32, D = 128 need about 1 MiB).  Larger requests return
+ *    WST_ERR_INVALID_ARG before anything is enqueued.
+ *  - The call allocates and frees nothing.  Its first call on a device looks
+ *    up the array's device address (cudaGetSymbolAddress); make that first
+ *    call before any stream capture.
+ *  - Every call on a device shares the one array and clears its header and
+ *    flags at the start: calls that can overlap on the GPU (other streams,
+ *    other host threads) race and must be serialised by the caller.
+ */
+wst_status wst_ikbo_linear_compress_noalloc(int num_users, int num_cand, int Du, int Dc,
+                                            int D, int O,
+                                            const void* U, const void* Cf, const void* W,
+                                            const int* d_user_offsets, void* Y,
+                                            int* d_status, void* stream);
 
 /* Synchronize `stream`, then return and clear the first device-side error
  * latched in `workspace` (WST_OK if none). */

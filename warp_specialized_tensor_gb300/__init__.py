@@ -21,7 +21,7 @@ __all__ = [
     "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "F32", "BF16",
     "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
     "workspace", "wst_gemm_bf16", "wst_grouped_gemm_bf16",
-    "wst_ikbo_linear_compress", "wst_sync_status", "wst_status_string",
+    "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_sync_status", "wst_status_string",
     "wst_version",
 ]
 
@@ -69,6 +69,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_grouped_gemm_bf16.restype = I
         lib.wst_ikbo_linear_compress.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
         lib.wst_ikbo_linear_compress.restype = I
+        lib.wst_ikbo_linear_compress_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
+        lib.wst_ikbo_linear_compress_noalloc.restype = I
         lib.wst_sync_status.argtypes = [P, P]
         lib.wst_sync_status.restype = I
         lib.wst_status_string.argtypes = [I]
@@ -242,6 +244,32 @@ def wst_ikbo_linear_compress(U, Cf, W, user_offsets, Y, workspace, stream=None) 
         users, cand, Du, Dc, D, O, U.data_ptr(), Cf.data_ptr(), W.data_ptr(),
         user_offsets.data_ptr(), Y.data_ptr(), workspace.data_ptr(), _stream_handle(stream))
     _check(st, "wst_ikbo_linear_compress")
+
+
+def wst_ikbo_linear_compress_noalloc(U, Cf, W, user_offsets, Y, status=None,
+                                     stream=None) -> None:
+    """wst_ikbo_linear_compress without a workspace, for callers that cannot
+    allocate device memory at call time: the scratch lives in a fixed 4 MiB
+    device array inside the library (shared by every call on the device, so
+    overlapping calls race).  status: optional device int32 tensor that
+    receives the call's device-side status code."""
+    for t, n, d in ((U, "U", 3), (Cf, "Cf", 3), (W, "W", 2)):
+        _need(t, n, torch.bfloat16, (d,))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    _need(Y, "Y", torch.float32, (3,))
+    _need(user_offsets, "user_offsets", torch.int32, (1,))
+    if status is not None:
+        _need(status, "status", torch.int32, (1,))
+    users, Du, D = U.shape
+    cand, Dc, D2 = Cf.shape
+    O, F = W.shape
+    if D2 != D or F != Du + Dc or Y.shape != (cand, O, D) or user_offsets.numel() != users + 1:
+        raise ValueError("shape mismatch")
+    st = load_library().wst_ikbo_linear_compress_noalloc(
+        users, cand, Du, Dc, D, O, U.data_ptr(), Cf.data_ptr(), W.data_ptr(),
+        user_offsets.data_ptr(), Y.data_ptr(), _ptr(status), _stream_handle(stream))
+    _check(st, "wst_ikbo_linear_compress_noalloc")
 
 
 def wst_sync_status(workspace, stream=None) -> int:

@@ -1,4 +1,6 @@
 // ikbo_ws.cu -- launcher of the IKBO linear-compression kernel.
+#include <mutex>
+
 #include "ikbo_ws.cuh"
 #include "wst_host.h"
 
@@ -118,6 +120,70 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, k_ikbo_ws, tmU, tmC, tmW, tmY, a);
   if (e != cudaSuccess) return cuda_fail(e, "launch k_ikbo_ws");
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (wst_ikbo_linear_compress_noalloc).
+//
+// Some callers cannot allocate device memory at call time: code that runs
+// under a strict memory budget or a custom allocator it must not bypass, or a
+// plugin whose host framework owns every allocation.  For them the same
+// kernel runs with its scratch (header, ready flags, per-user partial
+// products) in this file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_ikbo_scratch[kNoAllocScratchBytes];
+
+size_t ikbo_noalloc_capacity() { return kNoAllocScratchBytes; }
+
+// Device address of g_ikbo_scratch on the current device.  The host-side
+// symbol is only a stand-in, so the address is looked up once per device
+// (with that device current) and cached.
+static int ikbo_noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) {
+    set_error("device ordinal %d out of range", dev);
+    return ST_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_ikbo_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(ikbo scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return ST_OK;
+}
+
+int run_ikbo_noalloc(IkboProblem pr, int* d_status, cudaStream_t stream) {
+  const size_t need = workspace_bytes(pr.num_users, pr.O, pr.D);
+  if (need > kNoAllocScratchBytes) {
+    set_error("ikbo (allocation-free): %d users x O=%d x D=%d need %zu bytes of scratch; "
+              "this entry point holds %zu bytes (use wst_ikbo_linear_compress with a workspace)",
+              pr.num_users, pr.O, pr.D, need, kNoAllocScratchBytes);
+    return ST_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  int st = ikbo_noalloc_scratch(&scratch);
+  if (st) return st;
+  // The array keeps the previous call's contents: clear the header (error
+  // word, epoch) and the ready flags so this call starts from zero.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, ikbo_partials_offset(pr.num_users), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ikbo scratch)");
+  pr.ws = scratch;
+  st = run_ikbo(pr, stream);
+  if (st) return st;
+  if (d_status) {
+    e = cudaMemcpyAsync(d_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(status)");
+  }
   return ST_OK;
 }
 

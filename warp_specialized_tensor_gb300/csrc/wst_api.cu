@@ -333,6 +333,58 @@ wst_status wst_ikbo_linear_compress(int num_users, int num_cand, int Du, int Dc,
   return (wst_status)run_ikbo(p, static_cast<cudaStream_t>(stream));
 }
 
+wst_status wst_ikbo_linear_compress_noalloc(int num_users, int num_cand, int Du, int Dc, int D,
+                                            int O, const void* U, const void* Cf, const void* W,
+                                            const int* d_user_offsets, void* Y, int* d_status,
+                                            void* stream) {
+  g_err[0] = 0;
+  if (num_users < 1 || num_cand < 0 || Du < 1 || Dc < 1 || D < 1 || O < 1)
+    return fail(WST_ERR_INVALID_ARG, "sizes out of range (users=%d cand=%d Du=%d Dc=%d D=%d O=%d)",
+                num_users, num_cand, Du, Dc, D, O);
+  if (!U || !Cf || !W || !d_user_offsets || !Y)
+    return fail(WST_ERR_INVALID_ARG, "U, Cf, W, offsets and Y must be non-NULL");
+  if (D != 128) return fail(WST_ERR_UNSUPPORTED, "D=%d: this build supports D == 128", D);
+  if (O % 32 || O > 256) return fail(WST_ERR_UNSUPPORTED, "O=%d: needs a multiple of 32 up to 256", O);
+  if (Du % 8 || Dc % 8) return fail(WST_ERR_UNSUPPORTED, "Du=%d, Dc=%d: need multiples of 8", Du, Dc);
+  if (Du + Dc > 512) return fail(WST_ERR_UNSUPPORTED, "Du + Dc = %d > 512", Du + Dc);
+  if (workspace_bytes(num_users, O, D) > ikbo_noalloc_capacity())
+    return fail(WST_ERR_INVALID_ARG,
+                "%d users x O=%d x D=%d need %zu bytes of scratch; the allocation-free entry point "
+                "holds %zu bytes (use wst_ikbo_linear_compress with a workspace)",
+                num_users, O, D, workspace_bytes(num_users, O, D), ikbo_noalloc_capacity());
+  if (!aligned16(U) || !aligned16(Cf) || !aligned16(W) || !aligned16(Y) ||
+      (reinterpret_cast<uintptr_t>(d_user_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(d_status) & 3u))
+    return fail(WST_ERR_ALIGNMENT, "U, Cf, W, Y must be 16-byte aligned, offsets and status 4-byte");
+  WST_TRY(check_device_ptr(U, "U"));
+  WST_TRY(check_device_ptr(Cf, "Cf"));
+  WST_TRY(check_device_ptr(W, "W"));
+  WST_TRY(check_device_ptr(Y, "Y"));
+  WST_TRY(check_device_ptr(d_user_offsets, "d_user_offsets"));
+  if (d_status) WST_TRY(check_device_ptr(d_status, "d_status"));
+  if (num_cand == 0) {
+    if (d_status) {
+      cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int), static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return (wst_status)cuda_fail(e, "cudaMemsetAsync(status)");
+    }
+    return WST_OK;
+  }
+  IkboProblem p{};
+  p.num_users = num_users;
+  p.num_cand = num_cand;
+  p.Du = Du;
+  p.Dc = Dc;
+  p.D = D;
+  p.O = O;
+  p.U = U;
+  p.Cf = Cf;
+  p.W = W;
+  p.uoff = d_user_offsets;
+  p.Y = Y;
+  p.ws = nullptr;
+  return (wst_status)run_ikbo_noalloc(p, d_status, static_cast<cudaStream_t>(stream));
+}
+
 wst_status wst_sync_status(void* workspace, void* stream) {
   g_err[0] = 0;
   if (!workspace) return fail(WST_ERR_INVALID_ARG, "workspace is NULL");

@@ -70,5 +70,7 @@ struct IkboProblem {
 
 int run_gemm(const GemmProblem& p, cudaStream_t stream);
 int run_ikbo(const IkboProblem& p, cudaStream_t stream);
+int run_ikbo_noalloc(IkboProblem p, int* d_status, cudaStream_t stream);
+size_t ikbo_noalloc_capacity();
 
 }  // namespace wst
