@@ -73,6 +73,24 @@ def ikbo_bytes(users, cand, Du, Dc, D, O):
         (users + 1) * 4
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest value across ranks (every rank gets it); identity when
+    dist is None.  Used for the timed region: the job is as slow as its
+    slowest rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_flops: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs `steps` steps of `step_flops`."""
+    return step_flops * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -286,14 +304,9 @@ def run_ours(args, rank, world, dist):
     elapsed_ms = t_begin.elapsed_time(t_end)
     per_kernel_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n, _ in kernels}
 
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev if tdist.get_backend() == "nccl" else "cpu")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = job_throughput(step_flops, args.steps, world, elapsed_ms)
 
     # ---- e2e: host buffers in pinned memory, copies inside the timed region
     pinned = {n: t.pin_memory() for n, t in host.items()}
@@ -327,12 +340,9 @@ def run_ours(args, rank, world, dist):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev if tdist.get_backend() == "nccl" else "cpu")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = step_flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12 if e2e_steps else None
+    if e2e_steps:
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = job_throughput(step_flops, e2e_steps, world, e2e_ms) if e2e_steps else None
 
     # ---- context: cuBLAS through torch.matmul on the dense workload (not the product)
     ctx = {}
