@@ -360,6 +360,11 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize(dev)
         ctx["torch_matmul_dense_tflops"] = round(flops["dense"] * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e12, 1)
 
+    # ---- the two parity-only workloads, timed on their own (not in the step)
+    extra = {}
+    if not args.only and not args.no_extra:
+        extra = time_parity_workloads(wst, torch, dev, stream, peaks, ws)
+
     variants = {}
     for n, _ in kernels:
         ms = per_kernel_ms[n]
@@ -395,12 +400,56 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": len(kernels) * args.steps,
         "clocks": sampler.summary(),
         "variants": variants,
+        "parity_workloads": extra,
         "peaks": peaks,
         "context": ctx,
     }
     if rank == 0 and not args.no_cpu_baseline and not args.only:
         result["cpu_baseline"] = cpu_baseline(d, g, k, budget_s=args.cpu_seconds)
     return result
+
+
+def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20):
+    """dense 256^3 (fp32 out; launch-latency bound) and the skinny recsys
+    batch (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2)."""
+    import synthetic
+    out = {}
+    cases = []
+    d1 = synthetic.workload("dense256")
+    A1, B1 = d1["A"].to(dev), d1["B"].to(dev)
+    C1 = torch.empty(256, 256, dtype=torch.float32, device=dev)
+    cases.append(("dense256", lambda: wst.wst_gemm_bf16(A1, B1, C1, workspace=ws, stream=stream),
+                  dense_flops(256, 256, 256), dense_bytes(256, 256, 256, out_bytes=4)))
+    d5 = synthetic.workload("skinny_batch")
+    A5, B5, b5 = d5["A"].to(dev), d5["B"].to(dev), d5["bias"].to(dev)
+    C5 = torch.empty(512, 1024, 256, dtype=torch.bfloat16, device=dev)
+    cases.append(("skinny_batch",
+                  lambda: wst.wst_gemm_bf16(A5, B5, C5, bias=b5, epi="bias_silu", workspace=ws,
+                                            stream=stream),
+                  dense_flops(1024, 256, 512, batch=512),
+                  dense_bytes(1024, 256, 512, batch=512) + 512 * 256 * 2))
+    for name, fn, fl, by in cases:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / iters
+        t_flop = fl / (peaks["bf16_tflops"] * 1e12)
+        t_byte = by / (peaks["hbm_gbs"] * 1e9)
+        out[name] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                     "gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                     "bound": "tensor" if t_flop >= t_byte else "hbm",
+                     "frac_roofline": round(max(t_flop, t_byte) / (ms * 1e-3), 4)}
+    st = wst.wst_sync_status(ws, stream)
+    if st != 0:
+        raise RuntimeError("device error in parity workloads: %s" % wst.wst_status_string(st))
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -524,6 +573,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip timing the two parity-only workloads")
     ap.add_argument("--only", choices=["dense", "grouped", "ikbo"], default=None,
                     help="time one kernel only (profiling runs); not a bench line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

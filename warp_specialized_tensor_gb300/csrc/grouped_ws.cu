@@ -24,10 +24,10 @@ int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t st
       return st;
   }
   {
-    // token rows of A, K contiguous: {K, M_total}
+    // token rows of A, K contiguous: {K, M_total}, 32-row boxes
     uint64_t dims[2] = {(uint64_t)pr.K, (uint64_t)pr.M};
     uint64_t str[1] = {(uint64_t)pr.lda * 2};
-    uint32_t box[2] = {64, 128};
+    uint32_t box[2] = {64, (uint32_t)kGrpXBoxRows};
     if ((st = encode_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.A, dims, str, box,
                          CU_TENSOR_MAP_SWIZZLE_128B)))
       return st;

@@ -8,9 +8,11 @@
 // ("swap AB"): the expert's output features n sit on the 256-row MMA side
 // (two CTAs x 128 TMEM lanes), and the tokens of the group sit on the MMA's N
 // side, whose size is a multiple of 16 up to 256.  A group of T tokens is cut
-// into ceil(T/256) token tiles whose last one is only rounded up to 16, so a
-// ragged group wastes at most 15 token columns instead of up to 127 rows of a
-// 128-row tile.  Both operands are K-major in memory, as the hardware wants.
+// into ceil(T/256) token tiles of (nearly) equal width, rounded up to 16, so a
+// ragged group wastes at most 15 token columns per tile instead of up to 127
+// rows of a 128-row tile, and no tile is a thin, load-bound remainder.  Token
+// rows are fetched in 32-row boxes, only as many as the tile needs.  Both
+// operands are K-major in memory, as the hardware wants.
 //
 // Roles per CTA (persistent, one CTA per SM, pairs in clusters of 2):
 //   warp 0     TMA producer: this CTA's 128 rows of B[g] and its half of the
@@ -44,7 +46,9 @@ constexpr int kGrpStages = 6;
 constexpr int kGrpEpiWarps = 4;
 constexpr int kGrpThreads = 128 + 32 * kGrpEpiWarps;
 constexpr int kGrpWBytes = 128 * kGrpBK * 2;   // this CTA's 128 rows of B[g]
-constexpr int kGrpXBytes = 128 * kGrpBK * 2;   // up to 128 token rows (box height)
+constexpr int kGrpXBytes = 128 * kGrpBK * 2;   // up to 128 token rows per CTA
+constexpr int kGrpXBoxRows = 32;               // token rows per TMA box
+constexpr int kGrpXBoxBytes = kGrpXBoxRows * kGrpBK * 2;
 constexpr int kGrpStageBytes = kGrpWBytes + kGrpXBytes;
 constexpr int kGrpStgBytes = 32 * 32 * 4;      // per-warp transpose buffer (fp32 worst case)
 constexpr size_t kGrpSmemBytes = (size_t)kGrpStages * kGrpStageBytes +
@@ -77,7 +81,7 @@ struct GrpTile {
 struct GrpWalker {
   int g;
   long long base, count;
-  int r0, r1, tt;
+  int r0, r1, tt, sz;  // rows, token tiles, token-tile width
 
   __device__ __forceinline__ void load(const GroupedArgs& p) {
     if (g >= p.G) { count = 0; return; }
@@ -88,6 +92,8 @@ struct GrpWalker {
     r0 = a;
     r1 = b;
     tt = (b - a + kGrpTileT - 1) / kGrpTileT;
+    // equal widths: ceil(T / tt) rounded up to 16 (<= 256)
+    sz = tt ? ((((b - a) + tt - 1) / tt + 15) & ~15) : 0;
     count = (long long)tt * p.n_tiles;
   }
   __device__ __forceinline__ void init(const GroupedArgs& p) {
@@ -110,8 +116,8 @@ struct GrpWalker {
     const int nt_i = r - tok * p.n_tiles;
     GrpTile x;
     x.g = g;
-    x.t0 = r0 + tok * kGrpTileT;
-    x.nt = min(kGrpTileT, r1 - x.t0);
+    x.t0 = r0 + tok * sz;
+    x.nt = min(sz, r1 - x.t0);
     x.nmma = (x.nt + 15) & ~15;
     x.n0 = nt_i * kGrpTileN;
     return x;
@@ -195,17 +201,21 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const GrpTile tl = gw.tile(p, t);
         const int w_row = tl.n0 + (int)rank * 128;
         const int x_row = tl.t0 + (int)rank * (tl.nmma >> 1);
+        const int x_boxes = ((tl.nmma >> 1) + kGrpXBoxRows - 1) / kGrpXBoxRows;
+        const uint32_t tx = 2u * (uint32_t)(kGrpWBytes + x_boxes * kGrpXBoxBytes);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase_cluster(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * kGrpStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
           const uint32_t fb = map_to_cta(full_bar(stage), 0);
           const int kx = kb * kGrpBK;
           tma_load_3d_pair(smem_addr(smW + stage * kGrpWBytes), &tmW, fb, kx, w_row,
                            p.w_shared ? 0 : tl.g);
-          tma_load_2d_pair(smem_addr(smX + stage * kGrpXBytes), &tmX, fb, kx, x_row);
+          const uint32_t xdst = smem_addr(smX + stage * kGrpXBytes);
+          for (int i = 0; i < x_boxes; ++i)
+            tma_load_2d_pair(xdst + i * kGrpXBoxBytes, &tmX, fb, kx, x_row + i * kGrpXBoxRows);
           if (++stage == kGrpStages) { stage = 0; phase ^= 1u; }
         }
       }

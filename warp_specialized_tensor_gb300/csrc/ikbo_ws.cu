@@ -22,7 +22,7 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   a.kb_u = (pr.Du + 63) / 64;
   a.kb_c = (pr.Dc + 63) / 64;
   const size_t w_bytes = align_up((size_t)(a.kb_u + a.kb_c) * pr.O * 128, 1024);
-  const size_t fixed = w_bytes + 4 * 2 * kIkboStgBytes /*output staging*/ +
+  const size_t fixed = w_bytes + kIkboStgTotal /*output staging*/ +
                        1024 /*barriers, flags*/ + 1024 /*alignment slack*/;
   const size_t smem_cap = dev.max_smem_optin > 0 ? (size_t)dev.max_smem_optin : 232448;
   if (fixed + 4 * (size_t)kIkboABytes > smem_cap) {

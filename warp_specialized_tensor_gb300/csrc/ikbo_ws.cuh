@@ -36,10 +36,14 @@ namespace wst {
 
 constexpr int kIkboMaxStages = 12;
 constexpr int kIkboMaxSlots = 16;
-constexpr int kIkboThreads = 256;  // warps 0-3 roles, 4-7 epilogue
+constexpr int kIkboEpiGroups = 2;  // epilogue warpgroups, alternating over items
+constexpr int kIkboThreads = 128 + 128 * kIkboEpiGroups;  // warps 0-3 roles, 4.. epilogue
 constexpr int kIkboABytes = 128 * 64 * 2;  // one K-block of U^T / Cf^T: 64 f x 128 d
 constexpr int kIkboMaxGrid = 256;          // CTAs (<= SMs) the candidate split covers
 constexpr int kIkboStgBytes = 32 * 32 * 4; // per-warp output staging: 32 o x 32 d fp32
+// All output staging of a CTA (one buffer per epilogue warp); the launcher
+// sizes shared memory with the same constant.
+constexpr int kIkboStgTotal = 4 * kIkboEpiGroups * kIkboStgBytes;
 
 struct IkboArgs {
   int num_users, num_cand, Du, Dc, D, O;
@@ -78,8 +82,8 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   const int w_kb_bytes = p.O * 128;  // one K-block of W^T: O rows x 128 B
   uint8_t* smW = smem;
   uint8_t* smA = smW + align_up((size_t)kb_w * w_kb_bytes, 1024);
-  uint8_t* smY = smA + (size_t)p.stages * kIkboABytes;  // 4 warps x 2 x 4 KB output staging
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smY + 4 * 2 * kIkboStgBytes);
+  uint8_t* smY = smA + (size_t)p.stages * kIkboABytes;  // one 4 KB staging buffer per epilogue warp
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smY + kIkboStgTotal);
   // bars: full[stages] | empty[stages] | accf[slots] | acce[slots] | w
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
   uint32_t* tmem_slot = misc;                       // [0]
@@ -211,12 +215,13 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    // Two warpgroups take alternate items, so one drains its accumulator and
+    // stores while the other waits for the next: the per-item epilogue
+    // latency is overlapped instead of serialised.
+    const int grp = (warp - 4) >> 2;
     const int d = q * 32 + (int)lane;  // embedding position = TMEM lane
     const int nchunk = p.O / 32;
-    int slot = 0;
-    uint32_t slot_phase = 0;
     int cached_user = -1;
-    int ybuf = 0;
     int ucur = 0;  // user cursor for the candidate range
     float pc[2][32];
     if (c_lo < c_hi) {
@@ -228,7 +233,9 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
       }
       ucur = lo;
     }
-    for (int it = 0; it < n_items; ++it) {
+    for (int it = grp; it < n_items; it += kIkboEpiGroups) {
+      const int slot = it % p.slots;
+      const uint32_t slot_phase = (uint32_t)(it / p.slots) & 1u;
       const bool is_user = it < n_user_items;
       const int idx = is_user ? (int)blockIdx.x + it * (int)gridDim.x : c_lo + (it - n_user_items);
       if (!is_user) {
@@ -288,8 +295,8 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
           }
           // Stage this warp's 32 o x 32 d block (row o = 128 B, lane = d) and
           // TMA-store it to Y[idx][32j .. 32j+31][32q .. 32q+31].
-          uint8_t* sb = smY + ((q * 2 + ybuf) * kIkboStgBytes);
-          if (lane == 0) bulk_wait_group_read<1>();
+          uint8_t* sb = smY + (warp - 4) * kIkboStgBytes;
+          if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
           const uint32_t base = smem_addr(sb) + lane * 4u;
 #pragma unroll
@@ -301,13 +308,11 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
             tma_store_2d(&tmY, smem_addr(sb), q * 32, idx * p.O + j * 32);
             bulk_commit_group();
           }
-          ybuf ^= 1;
         }
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(slot));
-      if (++slot == p.slots) { slot = 0; slot_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();

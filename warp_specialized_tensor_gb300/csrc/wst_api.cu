@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/wst.h"
+#include "wst.h"
 #include "wst_common.cuh"
 #include "wst_host.h"
 
