@@ -8,10 +8,11 @@
 // ("swap AB"): the expert's output features n sit on the 256-row MMA side
 // (two CTAs x 128 TMEM lanes), and the tokens of the group sit on the MMA's N
 // side, whose size is a multiple of 16 up to 256.  A group of T tokens is cut
-// into ceil(T/256) token tiles of (nearly) equal width, rounded up to 16, so a
-// ragged group wastes at most 15 token columns per tile instead of up to 127
-// rows of a 128-row tile, and no tile is a thin, load-bound remainder.  Token
-// rows are fetched in 32-row boxes, only as many as the tile needs.  Both
+// into 256-token tiles and one remainder tile rounded up to 16, so a ragged
+// group wastes at most 15 token columns instead of up to 127 rows of a
+// 128-row tile.  (Measured on GB300 against equal-width token tiles and
+// against fetching token rows in 32-row boxes: both were slower than this
+// layout, which fetches each CTA's token rows as one 128-row box.)  Both
 // operands are K-major in memory, as the hardware wants.
 //
 // Roles per CTA (persistent, one CTA per SM, pairs in clusters of 2):
@@ -47,7 +48,7 @@ constexpr int kGrpEpiWarps = 4;
 constexpr int kGrpThreads = 128 + 32 * kGrpEpiWarps;
 constexpr int kGrpWBytes = 128 * kGrpBK * 2;   // this CTA's 128 rows of B[g]
 constexpr int kGrpXBytes = 128 * kGrpBK * 2;   // up to 128 token rows per CTA
-constexpr int kGrpXBoxRows = 32;               // token rows per TMA box
+constexpr int kGrpXBoxRows = 128;              // token rows per TMA box (one box per CTA)
 constexpr int kGrpXBoxBytes = kGrpXBoxRows * kGrpBK * 2;
 constexpr int kGrpStageBytes = kGrpWBytes + kGrpXBytes;
 constexpr int kGrpStgBytes = 32 * 32 * 4;      // per-warp transpose buffer (fp32 worst case)
@@ -92,8 +93,7 @@ struct GrpWalker {
     r0 = a;
     r1 = b;
     tt = (b - a + kGrpTileT - 1) / kGrpTileT;
-    // equal widths: ceil(T / tt) rounded up to 16 (<= 256)
-    sz = tt ? ((((b - a) + tt - 1) / tt + 15) & ~15) : 0;
+    sz = kGrpTileT;
     count = (long long)tt * p.n_tiles;
   }
   __device__ __forceinline__ void init(const GroupedArgs& p) {

@@ -36,14 +36,18 @@ namespace wst {
 
 constexpr int kIkboMaxStages = 12;
 constexpr int kIkboMaxSlots = 16;
-constexpr int kIkboEpiGroups = 2;  // epilogue warpgroups, alternating over items
+// One epilogue warpgroup (measured on GB300: two warpgroups taking alternate
+// items were slower, 72 vs 66 us on the 64 x 128 workload).
+constexpr int kIkboEpiGroups = 1;
 constexpr int kIkboThreads = 128 + 128 * kIkboEpiGroups;  // warps 0-3 roles, 4.. epilogue
 constexpr int kIkboABytes = 128 * 64 * 2;  // one K-block of U^T / Cf^T: 64 f x 128 d
 constexpr int kIkboMaxGrid = 256;          // CTAs (<= SMs) the candidate split covers
 constexpr int kIkboStgBytes = 32 * 32 * 4; // per-warp output staging: 32 o x 32 d fp32
-// All output staging of a CTA (one buffer per epilogue warp); the launcher
-// sizes shared memory with the same constant.
-constexpr int kIkboStgTotal = 4 * kIkboEpiGroups * kIkboStgBytes;
+// Output staging buffers per epilogue warp (double-buffered when each warp
+// handles every item) and in total; the launcher sizes shared memory with
+// the same constant.
+constexpr int kIkboStgPerWarp = kIkboEpiGroups == 1 ? 2 : 1;
+constexpr int kIkboStgTotal = 4 * kIkboEpiGroups * kIkboStgPerWarp * kIkboStgBytes;
 
 struct IkboArgs {
   int num_users, num_cand, Du, Dc, D, O;
@@ -82,7 +86,7 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   const int w_kb_bytes = p.O * 128;  // one K-block of W^T: O rows x 128 B
   uint8_t* smW = smem;
   uint8_t* smA = smW + align_up((size_t)kb_w * w_kb_bytes, 1024);
-  uint8_t* smY = smA + (size_t)p.stages * kIkboABytes;  // one 4 KB staging buffer per epilogue warp
+  uint8_t* smY = smA + (size_t)p.stages * kIkboABytes;  // output staging (kIkboStgTotal bytes)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smY + kIkboStgTotal);
   // bars: full[stages] | empty[stages] | accf[slots] | acce[slots] | w
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
@@ -215,10 +219,7 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    // Two warpgroups take alternate items, so one drains its accumulator and
-    // stores while the other waits for the next: the per-item epilogue
-    // latency is overlapped instead of serialised.
-    const int grp = (warp - 4) >> 2;
+    const int grp = (warp - 4) >> 2;  // epilogue warpgroup; groups take alternate items
     const int d = q * 32 + (int)lane;  // embedding position = TMEM lane
     const int nchunk = p.O / 32;
     int cached_user = -1;
@@ -295,8 +296,12 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
           }
           // Stage this warp's 32 o x 32 d block (row o = 128 B, lane = d) and
           // TMA-store it to Y[idx][32j .. 32j+31][32q .. 32q+31].
-          uint8_t* sb = smY + (warp - 4) * kIkboStgBytes;
-          if (lane == 0) bulk_wait_group_read<0>();
+          const int sbuf = kIkboStgPerWarp == 2 ? ((it / kIkboEpiGroups) * nchunk + j) & 1 : 0;
+          uint8_t* sb = smY + ((warp - 4) * kIkboStgPerWarp + sbuf) * kIkboStgBytes;
+          if (lane == 0) {
+            if (kIkboStgPerWarp == 2) bulk_wait_group_read<1>();
+            else bulk_wait_group_read<0>();
+          }
           __syncwarp();
           const uint32_t base = smem_addr(sb) + lane * 4u;
 #pragma unroll
