@@ -86,6 +86,7 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   a.c_stride = pr.strideC;
   a.ws = static_cast<WsHeader*>(pr.ws);
   a.timeout_ns = wait_timeout_ns();
+  a.inject_drop_load = take_fault_injection() ? 1 : 0;
 
   // Persistent grid: one CTA (pair) per SM (pair) that can be resident.
   long long grid = dev.num_sms;
@@ -104,9 +105,8 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
       ca[0].val.clusterDim.z = 1;
       q.attrs = ca;
       q.numAttrs = 1;
-      cudaError_t qe = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)Cfg::kSmemBytes);
-      if (qe != cudaSuccess) return cuda_fail(qe, "cudaFuncSetAttribute(gemm)");
+      if ((st = ensure_smem_attr((const void*)kern, Cfg::kSmemBytes))) return st;
+      cudaError_t qe;
       int n = 0;
       qe = cudaOccupancyMaxActiveClusters(&n, kern, &q);
       if (qe != cudaSuccess || n < 1) {
@@ -121,9 +121,8 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   if (grid < CG) grid = CG;
 
   // ---- launch
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Cfg::kSmemBytes);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
+  if ((st = ensure_smem_attr((const void*)kern, Cfg::kSmemBytes))) return st;
+  cudaError_t e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);

@@ -47,6 +47,7 @@ struct GemmArgs {
   long long c_stride;     // batch stride of C in elements (dense batched)
   WsHeader* ws;
   unsigned long long timeout_ns;
+  int inject_drop_load;   // test hook: CTA 0 skips its first K-block's loads
 };
 
 struct Tile {
@@ -217,6 +218,12 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
           if (!got) {
             ok = false;
             break;
+          }
+          if (p.inject_drop_load && blockIdx.x == 0 && t == cluster_id && kb == 0) {
+            // Fault-injection test hook: leave this slot's full barrier
+            // unarmed and unfilled, so the MMA issuer's bounded wait runs out.
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            continue;
           }
           // The leader's full[s] expects both CTAs' bytes; the peer only
           // contributes its copies' completions.

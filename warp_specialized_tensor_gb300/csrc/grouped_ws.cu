@@ -46,9 +46,8 @@ int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t st
   a.ws = static_cast<WsHeader*>(pr.ws);
   a.timeout_ns = wait_timeout_ns();
 
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kGrpSmemBytes);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped)");
+  if ((st = ensure_smem_attr((const void*)kern, kGrpSmemBytes))) return st;
+  cudaError_t e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

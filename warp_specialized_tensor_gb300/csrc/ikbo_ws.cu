@@ -78,9 +78,8 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   }
 
   const size_t smem = fixed + (size_t)stages * kIkboABytes;
-  cudaError_t e = cudaFuncSetAttribute(k_ikbo_ws, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ikbo)");
+  if ((st = ensure_smem_attr((const void*)k_ikbo_ws, smem))) return st;
+  cudaError_t e;
   int grid = dev.num_sms < kIkboMaxGrid ? dev.num_sms : kIkboMaxGrid;
   const long long items = (long long)pr.num_users + pr.num_cand;
   if (items < grid) grid = (int)items;

@@ -4,11 +4,14 @@
 // Every entry point validates on the host and returns a status before
 // anything is enqueued; nothing here throws, aborts, allocates device memory
 // or runs any part of the computation on the CPU.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "wst.h"
 #include "wst_common.cuh"
@@ -79,6 +82,30 @@ unsigned long long wait_timeout_ns() {
     return (unsigned long long)ms * 1000000ull;
   }();
   return v;
+}
+
+bool take_fault_injection() {
+  static const bool armed = [] {
+    const char* s = std::getenv("WST_FAULT_INJECT");
+    return s && std::strcmp(s, "drop_load") == 0;
+  }();
+  static std::atomic<int> used{0};
+  return armed && used.fetch_add(1) == 0;
+}
+
+int ensure_smem_attr(const void* kernel, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& have = done[std::make_pair(kernel, dev)];
+  if (have >= bytes) return ST_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  have = bytes;
+  return ST_OK;
 }
 
 int encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,

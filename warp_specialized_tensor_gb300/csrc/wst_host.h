@@ -34,6 +34,18 @@ int current_device_info(DeviceInfo* out);  // Status
 
 unsigned long long wait_timeout_ns();
 
+// Test hook for the bounded-wait error path: when the environment variable
+// WST_FAULT_INJECT=drop_load is set, the first dense GEMM launch of the
+// process (only that one) leaves one K-block unloaded, so its MMA issuer's
+// bounded wait runs out and the call latches WST_ERR_TIMEOUT.  No fault,
+// trap or hang: the kernel exits cleanly and later calls are normal.
+bool take_fault_injection();
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (cached: the attribute call is made once per kernel,
+// device and size).  Returns Status.
+int ensure_smem_attr(const void* kernel, size_t bytes);
+
 // Encode a tiled tensor map (rank 2 or 3).  dims / box innermost first,
 // strides_bytes has rank-1 entries.  Returns Status.
 int encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
