@@ -191,7 +191,6 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      if (blockIdx.x == 0) grouped_check_offsets(p);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -262,6 +261,10 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
     }
+  } else if (warp == 3) {
+    // Otherwise idle: validate the device offsets off the producers'
+    // critical path (one pass, latches WST_ERR_BAD_OFFSETS).
+    if (lane == 0 && blockIdx.x == 0) grouped_check_offsets(p);
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;

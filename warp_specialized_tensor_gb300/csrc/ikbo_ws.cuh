@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      if (blockIdx.x == 0) ikbo_check_offsets(p);
       // W^T, resident for the whole kernel.
       mbar_arrive_expect_tx(w_bar, (uint32_t)(kb_w * w_kb_bytes));
       for (int j = 0; j < kb_w; ++j) {
@@ -216,6 +215,10 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
         if (++slot == p.slots) { slot = 0; slot_phase ^= 1u; }
       }
     }
+  } else if (warp == 3) {
+    // Otherwise idle: validate the device offsets off the producers'
+    // critical path (one pass, latches WST_ERR_BAD_OFFSETS).
+    if (lane == 0 && blockIdx.x == 0) ikbo_check_offsets(p);
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -268,14 +271,19 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) __stcg(pu + (size_t)(j * 32 + i) * p.D + d, v[i]);
         }
-        // Publish P[u]: the last of the four epilogue warps to finish its
-        // rows releases flag[u] = this call's epoch.
-        __threadfence();
+        // Publish P[u]: __syncwarp orders the lanes' stores before lane 0's
+        // GPU-scope release fence; the fence and the shared-memory counter
+        // form a release pattern, so the last of the four warps to count in
+        // (after its own fence) releases flag[u] = this call's epoch with
+        // every warp's stores ordered before it.  One fence per warp, not
+        // one per thread: 128 fences in a row under a full memory system
+        // delayed the flag by ~10 us.
         __syncwarp();
         if (lane == 0) {
+          fence_acq_rel_gpu();
           const uint32_t old = atomicAdd(cnt + slot, 1u);
           if ((old & 3u) == 3u) {
-            __threadfence();
+            fence_acq_rel_gpu();
             st_release_gpu(p.flags + idx, target);
           }
         }
