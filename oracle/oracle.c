@@ -114,6 +114,48 @@ void oracle_gemm(int batch, int M, int N, int K,
 }
 
 /*
+ * GEMM on RMS-normalised rows of A (norm fused into the GEMM; any learned
+ * per-feature scale is taken as already folded into B):
+ *   r[b][m]    = 1 / sqrt( (1/K) sum_k A[b][m][k]^2 + eps )
+ *   C[b][m][n] = epi( r[b][m] * sum_k A[b][m][k] * B[b][n][k] (+ bias[b][n]) )
+ * Same argument conventions as oracle_gemm, plus eps.  The pages only name
+ * "norm fusion into GEMM" (a companion post of "How We Built TLX: A
+ * Hardware-Native GPU Compiler for Production ML at Scale"); this is the
+ * plainest RMSNorm reading.
+ */
+void oracle_gemm_rmsnorm(int batch, int M, int N, int K,
+                         const uint16_t *A, long lda, long sA,
+                         const uint16_t *B, long ldb, long sB, double eps,
+                         const uint16_t *bias, long sBias, int epi,
+                         double *C, long ldc, long sC,
+                         const int *rows, int nrows)
+{
+    long nr = rows ? nrows : M;
+    long total = (long)batch * nr;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (long idx = 0; idx < total; ++idx) {
+        int b = (int)(idx / nr);
+        int m = rows ? rows[idx % nr] : (int)(idx % nr);
+        const uint16_t *a = A + (long)b * sA + (long)m * lda;
+        const uint16_t *bias_row = bias ? bias + (long)b * sBias : 0;
+        double *c = C + (long)b * sC + (long)m * ldc;
+        double ss = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double x = bf16_to_double(a[k]);
+            ss += x * x;
+        }
+        double r = 1.0 / sqrt(ss / (double)K + eps);
+        for (int n = 0; n < N; ++n) {
+            const uint16_t *bn = B + (long)b * sB + (long)n * ldb;
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k)
+                acc += bf16_to_double(a[k]) * bf16_to_double(bn[k]);
+            c[n] = apply_epilogue(r * acc, epi, bias_row, n);
+        }
+    }
+}
+
+/*
  * Grouped GEMM: group g owns rows [off[g], off[g+1]) of A and C and uses
  * weight matrix B[g] (N x K, K contiguous, at B + g*sBg).  Empty groups
  * contribute nothing.  bias (if epi > 0) is per group: bias + g*sBias.

@@ -314,3 +314,49 @@ def test_ikbo_candidate_sample_and_bad_offsets():
     assert np.isnan(part[[0, 2]]).all()
     with pytest.raises(ValueError):
         oracle.ikbo(bf16_bits(U), bf16_bits(C), bf16_bits(W), [0, 3, 2])
+
+
+# ----------------------------------------------------------------------------
+# GEMM on RMS-normalised rows of A
+# ----------------------------------------------------------------------------
+def test_rmsnorm_constant_rows_closed_form():
+    # A row of constant value c has mean square c^2, so with eps = 0 the
+    # normalised row is sign(c) * 1 and C[m][n] = sign(c) * sum_k B[n][k].
+    K = 16
+    u = np.array([2.0, -0.5, 4.0])
+    A = np.repeat(u[:, None], K, axis=1)
+    rng = np.random.default_rng(61)
+    B = small_ints(rng, (5, K))
+    C = oracle.gemm_rmsnorm(bf16_bits(A), bf16_bits(B), eps=0.0)
+    ref = np.sign(u)[:, None] * B.sum(axis=1)[None, :]
+    np.testing.assert_allclose(C, ref, rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_scale_invariance_and_unit_rows():
+    g = torch.Generator().manual_seed(62)
+    A = torch.randn(6, 32, generator=g).to(torch.bfloat16)
+    B = torch.randn(7, 32, generator=g).to(torch.bfloat16)
+    C1 = oracle.gemm_rmsnorm(A, B, eps=0.0)
+    # scaling rows by powers of two is exact in bf16 and leaves C unchanged at eps = 0
+    scale = torch.tensor([1, 2, 4, 0.5, 8, 0.25]).to(torch.bfloat16)[:, None]
+    C2 = oracle.gemm_rmsnorm((A.float() * scale.float()).to(torch.bfloat16), B, eps=0.0)
+    np.testing.assert_allclose(C1, C2, rtol=1e-13, atol=1e-13)
+    # rows of +-1 have unit RMS: the normalised GEMM equals the plain GEMM
+    S = torch.where(torch.randn(6, 32, generator=g) > 0, 1.0, -1.0).to(torch.bfloat16)
+    np.testing.assert_allclose(oracle.gemm_rmsnorm(S, B, eps=0.0), oracle.gemm(S, B),
+                               rtol=1e-15, atol=1e-15)
+
+
+def test_rmsnorm_eps_and_epilogue():
+    # A = 0: r = 1/sqrt(eps) multiplies a zero product; the output is the (SiLU of the) bias
+    A = np.zeros((2, 8))
+    B = np.ones((3, 8))
+    bias = np.array([1.0, -2.0, 0.5])
+    C = oracle.gemm_rmsnorm(bf16_bits(A), bf16_bits(B), eps=1e-6, bias=bf16_bits(bias), epi="bias")
+    assert np.array_equal(C, np.tile(bias, (2, 1)))
+    # large eps: r ~ 1/sqrt(eps), so C ~ (A.B^T)/sqrt(eps)
+    rng = np.random.default_rng(63)
+    A = small_ints(rng, (3, 8), -2, 2)
+    B = small_ints(rng, (4, 8), -2, 2)
+    C = oracle.gemm_rmsnorm(bf16_bits(A), bf16_bits(B), eps=1e12)
+    np.testing.assert_allclose(C, (A @ B.T) / 1e6, rtol=1e-9, atol=1e-15)
