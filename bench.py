@@ -410,8 +410,9 @@ def run_ours(args, rank, world, dist):
 
 
 def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20):
-    """dense 256^3 (fp32 out; launch-latency bound) and the skinny recsys
-    batch (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2)."""
+    """dense 256^3 (fp32 out; launch-latency bound), the skinny recsys batch
+    (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2), and the
+    row-RMSNorm-fused GEMM on the dense 8192^3 operands."""
     import synthetic
     out = {}
     cases = []
@@ -428,6 +429,13 @@ def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20):
                                             stream=stream),
                   dense_flops(1024, 256, 512, batch=512),
                   dense_bytes(1024, 256, 512, batch=512) + 512 * 256 * 2))
+    # the fused row-RMSNorm GEMM on the dense 8192^3 operands (single-CTA tiles)
+    d2 = synthetic.workload("dense8192")
+    A2, B2 = d2["A"].to(dev), d2["B"].to(dev)
+    C2 = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev)
+    cases.append(("dense8192_rmsnorm",
+                  lambda: wst.wst_gemm_rmsnorm_bf16(A2, B2, C2, eps=1e-6, workspace=ws, stream=stream),
+                  dense_flops(8192, 8192, 8192), dense_bytes(8192, 8192, 8192)))
     for name, fn, fl, by in cases:
         for _ in range(3):
             fn()

@@ -112,6 +112,26 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K,
                          wst_epilogue epi, void* workspace, void* stream);
 
 /*
+ * GEMM on RMS-normalised rows of A (normalisation fused into the GEMM).  Same
+ * arguments, layouts and rules as wst_gemm_bf16, plus eps >= 0:
+ *   r[b][m]    = 1 / sqrt( (1/K) sum_k A[b][m][k]^2 + eps )
+ *   C[b][m][n] = epi( r[b][m] * sum_k A[b][m][k] * B[b][n][k] (+ bias[b][n]) )
+ * i.e. y = RMSNorm(x) W^T (+ b) with the norm's learned per-feature scale
+ * folded into B by the caller.  The row statistics are gathered from the A
+ * tiles as they stream through shared memory, so A is read from HBM once.
+ * Source: the TLX write-up ("How We Built TLX: A Hardware-Native GPU Compiler
+ * for Production ML at Scale", companion work on norm fusion into GEMMs, and
+ * "Five key areas": model-aware fusion); the pages give no formula, this is
+ * the plainest RMSNorm reading.  Runs on single-CTA 128 x 256 tiles.
+ */
+wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
+                                 const void* A, long lda, long strideA,
+                                 const void* B, long ldb, long strideB, float eps,
+                                 const void* bias, long strideBias,
+                                 void* C, long ldc, long strideC, wst_dtype c_type,
+                                 wst_epilogue epi, void* workspace, void* stream);
+
+/*
  * Grouped GEMM over G groups sharing N and K.  d_offsets is a DEVICE int32
  * array of G+1 entries, non-decreasing, d_offsets[0] = 0, d_offsets[G] =
  * M_total; group g owns rows [d_offsets[g], d_offsets[g+1]) of A and C

@@ -1,0 +1,92 @@
+"""GPU parity: GEMM on RMS-normalised rows of A (row statistics fused into the
+GEMM) vs the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import amax
+from oracle import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wst():
+    import warp_specialized_tensor_gb300 as w
+    w.load_library()
+    return w
+
+
+def rms_scale_max(A, eps):
+    a = A.float().numpy().astype(np.float64)
+    return float((1.0 / np.sqrt((a * a).mean(axis=-1) + eps)).max())
+
+
+def scaled_rows(M, N, K, batch=0, seed=0, bias=False):
+    """Rows of A with very different magnitudes, so the normalisation matters."""
+    d = synthetic.dense(M, N, K, batch=batch, seed=seed, bias=bias)
+    g = torch.Generator().manual_seed(seed + 1)
+    lead = (batch,) if batch else ()
+    s = torch.exp2(torch.randint(-4, 5, lead + (M, 1), generator=g).float())
+    d["A"] = (d["A"].float() * s).to(torch.bfloat16)
+    return d
+
+
+def run(wst, d, out, eps, epi="none"):
+    A, B = d["A"].cuda(), d["B"].cuda()
+    lead = (A.shape[0],) if A.dim() == 3 else ()
+    C = torch.full(lead + (A.shape[-2], B.shape[-2]), float("nan"), dtype=out, device="cuda")
+    bias = d["bias"].cuda() if epi != "none" else None
+    ws = wst.workspace()
+    wst.wst_gemm_rmsnorm_bf16(A, B, C, eps=eps, bias=bias, epi=epi, workspace=ws)
+    assert wst.wst_sync_status(ws) == 0
+    return C
+
+
+def check(C, d, eps, K, epi="none", rows=None):
+    ref = oracle.gemm_rmsnorm(d["A"], d["B"], eps=eps, bias=d.get("bias"), epi=epi, rows=rows)
+    g = C.float().cpu().numpy()
+    if rows is not None:
+        g, ref = g[..., rows, :], ref[..., rows, :]
+    s_r = rms_scale_max(d["A"], eps)
+    ok, metric, detail = compare.check(g, ref, K, amax(d["A"]) * s_r, amax(d["B"]),
+                                       C.dtype == torch.bfloat16)
+    assert ok, detail
+
+
+@pytest.mark.parametrize("M,N,K,out", [
+    (128, 256, 64, torch.float32),
+    (300, 520, 200, torch.bfloat16),
+    (513, 264, 1000, torch.float32),
+    (1, 8, 8, torch.float32),
+])
+def test_rmsnorm_shapes(wst, M, N, K, out):
+    d = scaled_rows(M, N, K, seed=M + N)
+    C = run(wst, d, out, 1e-6)
+    check(C, d, 1e-6, K)
+
+
+@pytest.mark.parametrize("epi,out", [("bias", torch.float32), ("bias_silu", torch.bfloat16)])
+def test_rmsnorm_batched_epilogue(wst, epi, out):
+    d = scaled_rows(300, 256, 512, batch=4, seed=71, bias=True)
+    C = run(wst, d, out, 1e-5, epi=epi)
+    check(C, d, 1e-5, 512, epi=epi)
+
+
+def test_rmsnorm_row_scale_invariance_bit_exact(wst):
+    # With eps = 0, doubling a row of A (exact in bf16) must leave C unchanged.
+    d = synthetic.dense(256, 256, 320, seed=72)
+    C1 = run(wst, d, torch.float32, 0.0)
+    d2 = dict(d)
+    d2["A"] = (d["A"].float() * 2.0).to(torch.bfloat16)
+    C2 = run(wst, d2, torch.float32, 0.0)
+    assert torch.equal(C1, C2)
+
+
+def test_rmsnorm_dense8192_sampled_rows(wst):
+    d = synthetic.workload("dense8192")
+    C = run(wst, d, torch.bfloat16, 1e-6)
+    rows = sorted(set(torch.randperm(8192, generator=torch.Generator().manual_seed(9))[:12].tolist() + [0, 8191]))
+    check(C, d, 1e-6, 8192, rows=rows)

@@ -20,7 +20,7 @@ from . import _build
 __all__ = [
     "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "F32", "BF16",
     "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
-    "workspace", "wst_gemm_bf16", "wst_grouped_gemm_bf16",
+    "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_grouped_gemm_bf16",
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_sync_status", "wst_status_string",
     "wst_version",
 ]
@@ -65,6 +65,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_workspace_init.restype = I
         lib.wst_gemm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, P, L, P, L, L, I, I, P, P]
         lib.wst_gemm_bf16.restype = I
+        lib.wst_gemm_rmsnorm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, ctypes.c_float, P, L,
+                                              P, L, L, I, I, P, P]
+        lib.wst_gemm_rmsnorm_bf16.restype = I
         lib.wst_grouped_gemm_bf16.argtypes = [I, I, I, I, P, L, P, L, L, P, P, L, P, L, I, I, P, P]
         lib.wst_grouped_gemm_bf16.restype = I
         lib.wst_ikbo_linear_compress.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
@@ -188,6 +191,38 @@ def wst_gemm_bf16(A, B, C, bias=None, epi="none", workspace=None, stream=None) -
         _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(-2), sC, _ctype(C), e,
         workspace.data_ptr(), _stream_handle(stream))
     _check(st, "wst_gemm_bf16")
+
+
+def wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, bias=None, epi="none", workspace=None,
+                          stream=None) -> None:
+    """C[b] = epi(diag(r[b]) . A[b] . B[b]^T (+ bias[b])), r = 1/sqrt(mean(A^2, -1) + eps).
+
+    Same tensor conventions as wst_gemm_bf16."""
+    _need(A, "A", torch.bfloat16, (2, 3))
+    _need(B, "B", torch.bfloat16, (2, 3))
+    _need(C, "C", None, (2, 3))
+    if workspace is None:
+        raise ValueError("workspace is required (see workspace())")
+    batch = A.shape[0] if A.dim() == 3 else 1
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-2]
+    if B.shape[-1] != K or C.shape[-2:] != (M, N):
+        raise ValueError("shape mismatch")
+    if (B.dim() == 3 and B.shape[0] != batch) or (C.dim() == 3 and C.shape[0] != batch):
+        raise ValueError("batch mismatch")
+    sA = A.stride(0) if A.dim() == 3 else 0
+    sB = B.stride(0) if B.dim() == 3 else 0
+    sC = C.stride(0) if C.dim() == 3 else 0
+    e = _epi(epi)
+    sBias = 0
+    if e != EPI_NONE:
+        _need(bias, "bias", torch.bfloat16, (1, 2))
+        sBias = bias.stride(0) if bias.dim() == 2 else 0
+    st = load_library().wst_gemm_rmsnorm_bf16(
+        batch, M, N, K, A.data_ptr(), A.stride(-2), sA, B.data_ptr(), B.stride(-2), sB,
+        float(eps), _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(-2), sC, _ctype(C),
+        e, workspace.data_ptr(), _stream_handle(stream))
+    _check(st, "wst_gemm_rmsnorm_bf16")
 
 
 def wst_grouped_gemm_bf16(A, B, offsets, C, bias=None, epi="none", workspace=None,

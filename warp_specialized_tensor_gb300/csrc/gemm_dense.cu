@@ -26,12 +26,14 @@ inline int dense_cta_group(int M) {
   return M > kBM ? 2 : 1;
 }
 
-template <bool OUT_F32, int EPI, int CG>
+template <bool OUT_F32, int EPI, int CG, bool NORM>
 int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
-  constexpr int EW = EPI == 2 ? 8 : 4;
+  // 8 epilogue warps for SiLU (exp-heavy), except with the row-statistics
+  // warps, where 4 keep the block at 384 threads.
+  constexpr int EW = (EPI == 2 && !NORM) ? 8 : 4;
   constexpr int kStages = stages_for<CG>();
-  using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, CG>;
-  auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, CG>;
+  using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, CG, NORM>;
+  auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, CG, NORM>;
 
   // ---- tensor maps
   CUtensorMap tmA, tmB, tmC;
@@ -87,6 +89,8 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   a.ws = static_cast<WsHeader*>(pr.ws);
   a.timeout_ns = wait_timeout_ns();
   a.inject_drop_load = take_fault_injection() ? 1 : 0;
+  a.eps = pr.eps;
+  a.inv_k = 1.0f / (float)pr.K;
 
   // Persistent grid: one CTA (pair) per SM (pair) that can be resident.
   long long grid = dev.num_sms;
@@ -140,19 +144,19 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   return ST_OK;
 }
 
-template <int CG>
+template <int CG, bool NORM>
 int dispatch(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t s) {
   if (pr.c_f32) {
     switch (pr.epi) {
-      case 0: return launch_cfg<true, 0, CG>(pr, dev, s);
-      case 1: return launch_cfg<true, 1, CG>(pr, dev, s);
-      default: return launch_cfg<true, 2, CG>(pr, dev, s);
+      case 0: return launch_cfg<true, 0, CG, NORM>(pr, dev, s);
+      case 1: return launch_cfg<true, 1, CG, NORM>(pr, dev, s);
+      default: return launch_cfg<true, 2, CG, NORM>(pr, dev, s);
     }
   }
   switch (pr.epi) {
-    case 0: return launch_cfg<false, 0, CG>(pr, dev, s);
-    case 1: return launch_cfg<false, 1, CG>(pr, dev, s);
-    default: return launch_cfg<false, 2, CG>(pr, dev, s);
+    case 0: return launch_cfg<false, 0, CG, NORM>(pr, dev, s);
+    case 1: return launch_cfg<false, 1, CG, NORM>(pr, dev, s);
+    default: return launch_cfg<false, 2, CG, NORM>(pr, dev, s);
   }
 }
 
@@ -165,7 +169,9 @@ int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   int st = current_device_info(&dev);
   if (st) return st;
   if (pr.grouped) return run_gemm_grouped(pr, dev, stream);
-  return dense_cta_group(pr.M) == 2 ? dispatch<2>(pr, dev, stream) : dispatch<1>(pr, dev, stream);
+  if (pr.norm) return dispatch<1, true>(pr, dev, stream);  // row statistics: single-CTA tiles
+  return dense_cta_group(pr.M) == 2 ? dispatch<2, false>(pr, dev, stream)
+                                    : dispatch<1, false>(pr, dev, stream);
 }
 
 }  // namespace wst

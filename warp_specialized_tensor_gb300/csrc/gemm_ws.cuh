@@ -48,6 +48,7 @@ struct GemmArgs {
   WsHeader* ws;
   unsigned long long timeout_ns;
   int inject_drop_load;   // test hook: CTA 0 skips its first K-block's loads
+  float eps, inv_k;       // row-RMS normalisation (NORM kernels only)
 };
 
 struct Tile {
@@ -119,9 +120,10 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG>
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, bool NORM>
 struct GemmCfg {
-  static constexpr int kThreads = 128 + 32 * EPI_WARPS;
+  static constexpr int kStatsWarps = NORM ? 4 : 0;     // row sum-of-squares warps
+  static constexpr int kThreads = 128 + 32 * EPI_WARPS + 32 * kStatsWarps;
   static constexpr int kTileM = kBM * CG;              // rows of one (cluster) tile
   static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows
   static constexpr int kBRows = BN / CG;               // this CTA's share of the B tile
@@ -133,35 +135,45 @@ struct GemmCfg {
   static constexpr int kColsPerChunk = OUT_F32 ? 32 : 64;
   static constexpr int kWarpCols = BN / (EPI_WARPS / 4);  // columns one epilogue warp drains
   static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kScaleBytes = NORM ? 2 * kBM * 4 : 0;  // per-row scales, 2 buffers
   static constexpr size_t kSmemBytes = (size_t)STAGES * kStageBytes +
-                                       (size_t)EPI_WARPS * kStageBufs * kStgBytes + 256 /*bars*/ +
-                                       1024 /*alignment slack*/;
+                                       (size_t)EPI_WARPS * kStageBufs * kStgBytes + kScaleBytes +
+                                       256 /*bars*/ + 1024 /*alignment slack*/;
   static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kWarpCols % kColsPerChunk == 0, "epilogue chunking");
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+  static_assert(!NORM || CG == 1, "row normalisation runs on single-CTA tiles");
 };
 
+// NORM: C = epi(r[m] * (A.B^T)[m][n] (+ bias)), r[m] = 1/sqrt(mean_k A[m][k]^2
+// + eps).  Four extra "stats" warps read every A stage from the ring (each
+// lane one row: eight 16-byte swizzled chunks per stage), accumulate the
+// row's sum of squares in fp32, release the stage together with the MMA, and
+// hand 1/sqrt(ss/K + eps) per row to the epilogue through a double-buffered
+// shared array.  The norm costs no extra pass over A in HBM.
+//
 // CG = 2: a cluster of two CTAs computes one 256 x BN tile with
 // tcgen05.mma.cta_group::2 issued by the even CTA (the leader).  Each CTA
 // loads its own 128 rows of A and its half of B's BN rows (no multicast);
 // both CTAs' loads complete on the leader's full[s]; the leader's commits
 // arrive on empty[s] / acc_full[a] in both CTAs; both epilogues arrive on the
 // leader's acc_empty[a]; each CTA drains its own 128 accumulator rows.
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG>
-__global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, bool NORM>
+__global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     k_gemm_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
-  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, CG>;
+  using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, CG, NORM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + STAGES * Cfg::kABytes;
   uint8_t* smStg = smB + STAGES * Cfg::kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smStg + EPI_WARPS * Cfg::kStageBufs * Cfg::kStgBytes);
-  // bars: full[STAGES] | empty[STAGES] | acc_full[2] | acc_empty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  float* row_scale = reinterpret_cast<float*>(smStg + EPI_WARPS * Cfg::kStageBufs * Cfg::kStgBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(row_scale) + Cfg::kScaleBytes);
+  // bars: full[STAGES] | empty[STAGES] | acc_full[2] | acc_empty[2] | scale_full[2] | scale_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 8);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -171,6 +183,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
   auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  auto sclf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 4 + a); };
+  auto scle_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 6 + a); };
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;   // CTA rank in the pair
   const long long cluster_id = blockIdx.x / CG;
   const long long num_clusters = gridDim.x / CG;
@@ -178,11 +192,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + Cfg::kStatsWarps);  // MMA commit (+ stats warps)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), CG * EPI_WARPS);
+      mbar_init(sclf_bar(a), 4);
+      mbar_init(scle_bar(a), EPI_WARPS);
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -297,6 +313,48 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
     }
+  } else if (NORM && warp >= 4 + EPI_WARPS) {
+    // ------------------------------------------------------------------ row statistics
+    const int r = (warp - 4 - EPI_WARPS) * 32 + (int)lane;  // CTA-local row of A
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
+      float ss = 0.0f;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!warp_wait_phase(guard, full_bar(stage), phase, (kRoleEpilogue << 16) | 0x400 | stage)) {
+          ok = false;
+          break;
+        }
+        (void)mbar_try_wait(full_bar(stage), phase);  // each lane acquires the completed phase
+        const uint32_t row_addr = smem_addr(smA + stage * Cfg::kABytes) + (uint32_t)r * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t w0, w1, w2, w3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(row_addr + ((uint32_t)(j ^ (r & 7)) << 4)));
+          const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (!warp_wait_phase(guard, scle_bar(acc), acc_phase ^ 1u, (kRoleEpilogue << 16) | 0x500 | acc)) break;
+      row_scale[acc * kBM + r] = rsqrtf(ss * p.inv_k + p.eps);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sclf_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int ew = warp - 4;              // 0 .. EPI_WARPS-1
@@ -321,16 +379,32 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
       const __nv_bfloat16* bias_row =
           EPI ? p.bias + (long long)tl.b * p.bias_stride : nullptr;
       const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      float scale = 1.0f;
+      if constexpr (NORM) {
+        if (!warp_wait_phase(guard, sclf_bar(acc), acc_phase, (kRoleEpilogue << 16) | 0x600 | acc)) break;
+        (void)mbar_try_wait(sclf_bar(acc), acc_phase);
+        scale = row_scale[acc * kBM + q * 32 + (int)lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(scle_bar(acc));
+      }
 
 #pragma unroll 1
       for (int c0 = col_begin; c0 < col_begin + Cfg::kWarpCols; c0 += Cfg::kColsPerChunk) {
         float v0[32];
         tmem_load32(t_lane + c0, v0);
+        if constexpr (NORM) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v0[j] *= scale;
+        }
         apply_bias_act<EPI>(v0, bias_row, tl.n0 + c0, p.N);
         uint32_t packed[16];
         float v1[32];
         if constexpr (!OUT_F32) {
           tmem_load32(t_lane + c0 + 32, v1);
+          if constexpr (NORM) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v1[j] *= scale;
+          }
           apply_bias_act<EPI>(v1, bias_row, tl.n0 + c0 + 32, p.N);
 #pragma unroll
           for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);

@@ -265,6 +265,63 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K, const void* A, long lda
   return (wst_status)run_gemm(p, static_cast<cudaStream_t>(stream));
 }
 
+wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K, const void* A, long lda,
+                                 long strideA, const void* B, long ldb, long strideB, float eps,
+                                 const void* bias, long strideBias, void* C, long ldc,
+                                 long strideC, wst_dtype c_type, wst_epilogue epi,
+                                 void* workspace, void* stream) {
+  g_err[0] = 0;
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return fail(WST_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  wst_status s = validate_common((int)epi, (int)c_type, workspace);
+  if (s) return s;
+  if (batch < 1 || M < 1 || N < 1 || K < 1)
+    return fail(WST_ERR_INVALID_ARG, "sizes must be >= 1 (batch=%d M=%d N=%d K=%d)", batch, M, N, K);
+  if (!A || !B || !C) return fail(WST_ERR_INVALID_ARG, "A, B and C must be non-NULL");
+  if (lda < K || ldb < K || ldc < N)
+    return fail(WST_ERR_INVALID_ARG, "leading dimensions too small (lda=%ld ldb=%ld ldc=%ld)", lda, ldb, ldc);
+  if (strideA < 0 || strideB < 0 || strideC < 0 || strideBias < 0)
+    return fail(WST_ERR_INVALID_ARG, "negative batch stride");
+  const long es = c_type == WST_F32 ? 4 : 2;
+  if (batch > 1 && strideC < (long)(M - 1) * ldc + N)
+    return fail(WST_ERR_INVALID_ARG, "strideC=%ld makes batch outputs overlap", strideC);
+  if (epi != WST_EPI_NONE && !bias) return fail(WST_ERR_INVALID_ARG, "epilogue needs a bias");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (epi && !aligned16(bias)))
+    return fail(WST_ERR_ALIGNMENT, "A, B, C and bias must be 16-byte aligned");
+  if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldc * es) % 16 || (strideA * 2) % 16 ||
+      (strideB * 2) % 16 || (strideC * es) % 16 || (epi && (strideBias * 2) % 16))
+    return fail(WST_ERR_ALIGNMENT, "leading dimensions and batch strides must be multiples of 16 bytes");
+  WST_TRY(check_device_ptr(A, "A"));
+  WST_TRY(check_device_ptr(B, "B"));
+  WST_TRY(check_device_ptr(C, "C"));
+  if (epi) WST_TRY(check_device_ptr(bias, "bias"));
+  WST_TRY(check_device_ptr(workspace, "workspace"));
+
+  GemmProblem p{};
+  p.grouped = 0;
+  p.batch = batch;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.A = A;
+  p.lda = lda;
+  p.strideA = batch > 1 ? strideA : 0;
+  p.B = B;
+  p.ldb = ldb;
+  p.strideB = batch > 1 ? strideB : 0;
+  p.bias = epi ? bias : nullptr;
+  p.strideBias = strideBias;
+  p.C = C;
+  p.ldc = ldc;
+  p.strideC = batch > 1 ? strideC : 0;
+  p.c_f32 = c_type == WST_F32;
+  p.epi = (int)epi;
+  p.offsets = nullptr;
+  p.ws = workspace;
+  p.norm = 1;
+  p.eps = eps;
+  return (wst_status)run_gemm(p, static_cast<cudaStream_t>(stream));
+}
+
 wst_status wst_grouped_gemm_bf16(int G, int M_total, int N, int K, const void* A, long lda,
                                  const void* B, long ldb, long strideB_group, const int* d_offsets,
                                  const void* bias, long strideBias, void* C, long ldc,

@@ -68,6 +68,8 @@ struct GemmProblem {
   int epi;
   const int* offsets;
   void* ws;
+  int norm;    // dense only: scale row m by 1/sqrt(mean_k A[m][k]^2 + eps)
+  float eps;
 };
 
 struct IkboProblem {
