@@ -1,4 +1,10 @@
-"""GPU parity: grouped (MoE expert) GEMM with device offsets vs the fp64 oracle."""
+"""GPU parity: grouped (MoE expert) GEMM with device offsets vs the fp64 oracle.
+
+Every test runs under both tile schedules: the static persistent walk and
+hardware cluster launch control (WST_GROUPED_SCHED=clc, read per call).
+"""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -15,6 +21,17 @@ def wst():
     import warp_specialized_tensor_gb300 as w
     w.load_library()
     return w
+
+
+@pytest.fixture(autouse=True, params=["static", "clc"])
+def sched(request):
+    old = os.environ.get("WST_GROUPED_SCHED")
+    os.environ["WST_GROUPED_SCHED"] = request.param
+    yield request.param
+    if old is None:
+        del os.environ["WST_GROUPED_SCHED"]
+    else:
+        os.environ["WST_GROUPED_SCHED"] = old
 
 
 def run_grouped(wst, d, out_dtype=torch.bfloat16, bias=None, epi="none", extra_rows=128):

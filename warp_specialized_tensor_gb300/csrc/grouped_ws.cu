@@ -1,4 +1,7 @@
 // grouped_ws.cu -- instantiations and launcher of the grouped (MoE) GEMM.
+#include <cstdlib>
+#include <cstring>
+
 #include "grouped_ws.cuh"
 #include "wst_host.h"
 
@@ -6,9 +9,17 @@ namespace wst {
 
 namespace {
 
-template <bool OUT_F32, int EPI>
+// Tile schedule: the static persistent walk unless WST_GROUPED_SCHED=clc
+// selects hardware cluster launch control (read on every call, so one process
+// can time or test both).
+inline bool grouped_use_clc() {
+  const char* s = std::getenv("WST_GROUPED_SCHED");
+  return s != nullptr && std::strcmp(s, "clc") == 0;
+}
+
+template <bool OUT_F32, int EPI, bool CLC>
 int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
-  auto kern = k_grouped_ws<OUT_F32, EPI>;
+  auto kern = k_grouped_ws<OUT_F32, EPI, CLC>;
   int st;
   CUtensorMap tmW, tmX;
   GroupedArgs a{};
@@ -59,20 +70,34 @@ int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t st
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Persistent grid: every CTA pair that can be resident at once.
-  static int max_clusters[64] = {0};
-  int& mc = max_clusters[dev.device & 63];
-  if (mc == 0) {
-    cfg.gridDim = dim3((unsigned)(dev.num_sms & ~1), 1, 1);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess || n < 1) {
-      cudaGetLastError();
-      n = dev.num_sms / 2;
+  long long pairs;
+  if (CLC) {
+    // One pair per tile.  The group sizes are on the device, so bound the
+    // tile count: sum_g ceil(M_g/256) <= floor(M_total/256) + min(G, M_total).
+    pairs = (long long)a.n_tiles *
+            ((long long)a.M_total / kGrpTileT + std::min<long long>(a.G, a.M_total));
+    if (pairs < 1) pairs = 1;  // pair 0 still validates the offsets
+    if (2 * pairs > 0x7fffffffLL) {
+      set_error("grouped GEMM: %lld tiles exceed the grid limit of cluster launch control", pairs);
+      return ST_UNSUPPORTED;
     }
-    mc = n;
+  } else {
+    // Persistent grid: every CTA pair that can be resident at once.
+    static int max_clusters[64] = {0};
+    int& mc = max_clusters[dev.device & 63];
+    if (mc == 0) {
+      cfg.gridDim = dim3((unsigned)(dev.num_sms & ~1), 1, 1);
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = dev.num_sms / 2;
+      }
+      mc = n;
+    }
+    pairs = mc;
   }
-  cfg.gridDim = dim3((unsigned)(2 * mc), 1, 1);
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a);
   if (e != cudaSuccess) return cuda_fail(e, "launch k_grouped_ws");
   return ST_OK;
@@ -80,19 +105,29 @@ int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t st
 
 }  // namespace
 
-int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
+namespace {
+
+template <bool CLC>
+int dispatch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
   if (pr.c_f32) {
     switch (pr.epi) {
-      case 0: return launch_grouped<true, 0>(pr, dev, stream);
-      case 1: return launch_grouped<true, 1>(pr, dev, stream);
-      default: return launch_grouped<true, 2>(pr, dev, stream);
+      case 0: return launch_grouped<true, 0, CLC>(pr, dev, stream);
+      case 1: return launch_grouped<true, 1, CLC>(pr, dev, stream);
+      default: return launch_grouped<true, 2, CLC>(pr, dev, stream);
     }
   }
   switch (pr.epi) {
-    case 0: return launch_grouped<false, 0>(pr, dev, stream);
-    case 1: return launch_grouped<false, 1>(pr, dev, stream);
-    default: return launch_grouped<false, 2>(pr, dev, stream);
+    case 0: return launch_grouped<false, 0, CLC>(pr, dev, stream);
+    case 1: return launch_grouped<false, 1, CLC>(pr, dev, stream);
+    default: return launch_grouped<false, 2, CLC>(pr, dev, stream);
   }
+}
+
+}  // namespace
+
+int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
+  return grouped_use_clc() ? dispatch_grouped<true>(pr, dev, stream)
+                           : dispatch_grouped<false>(pr, dev, stream);
 }
 
 }  // namespace wst

@@ -24,6 +24,8 @@
 //              accumulators; commits release ring slots / accumulators in
 //              both CTAs.
 //   warp 2     TMEM allocation (both CTAs, 512 columns).
+//   warp 3     lane 1 of CTA 0 validates the offsets; with the
+//              cluster-launch-control schedule, lane 0 is the tile scheduler.
 //   warps 4-7  epilogue: each warp drains its 32 feature lanes, 32 tokens at a
 //              time, adds bias / SiLU, transposes through a private shared
 //              buffer and writes whole 64-byte (bf16) / 128-byte (fp32) row
@@ -48,17 +50,20 @@ constexpr int kGrpEpiWarps = 4;
 constexpr int kGrpThreads = 128 + 32 * kGrpEpiWarps;
 constexpr int kGrpWBytes = 128 * kGrpBK * 2;   // this CTA's 128 rows of B[g]
 constexpr int kGrpXBytes = 128 * kGrpBK * 2;   // up to 128 token rows per CTA
-// Tile schedule.  Static (default): pair c takes tiles c, c + #pairs, ...
-// Dynamic (build with -DGRP_DYNAMIC=1): the leader CTA's warp 3 takes tile
-// indices from a global counter in the workspace and hands them to both CTAs
-// of the pair through a small shared-memory queue, so pairs that finish
-// early take more tiles.  Measured on GB300 for the 64-expert MoE workload,
-// the dynamic schedule was 1.5 % slower (0.308 vs 0.303 ms): the per-pair
-// finish times spread by ~7 %, less than the queue's added latency costs.
-#ifndef GRP_DYNAMIC
-#define GRP_DYNAMIC 0
-#endif
-constexpr int kGrpTQ = 6;  // tile-queue slots
+// Tile schedule (template parameter CLC):
+//  * static: the grid is one CTA pair per pair of SMs and pair c takes
+//    tiles c, c + #pairs, ... (every role walks the same sequence);
+//  * cluster launch control: the grid holds one pair per tile (an upper
+//    bound: the group sizes live on the device) and pair c starts on tile c.
+//    Warp 3 of the leader asks the hardware to cancel a pair that has not
+//    been launched yet (clusterlaunchcontrol.try_cancel, response multicast
+//    to both CTAs) and takes over its tile, until no pair is left to cancel
+//    or the cancelled pair's tile lies past the last tile.  Each CTA's
+//    scheduler lane hands the tiles to its own roles through a 2-slot
+//    shared-memory queue, so a pair claims at most one tile ahead of the one
+//    its tensor core is working on.  Pairs launched past the last tile
+//    count the tiles and exit at once.
+constexpr int kGrpTQ = 2;  // tile-queue slots
 constexpr int kGrpXBoxRows = 128;              // token rows per TMA box (one box per CTA)
 constexpr int kGrpXBoxBytes = kGrpXBoxRows * kGrpBK * 2;
 constexpr int kGrpStageBytes = kGrpWBytes + kGrpXBytes;
@@ -113,6 +118,7 @@ struct GrpWalker {
     load(p);
   }
   __device__ __forceinline__ bool seek(const GroupedArgs& p, long long t) {
+    if (t < base) init(p);
     while (g < p.G && t >= base + count) {
       base += count;
       ++g;
@@ -135,6 +141,26 @@ struct GrpWalker {
   }
 };
 
+// Number of tiles of the problem, with the walker's clamping; computed by a
+// whole warp (one group per lane and pass), every lane returns it.
+__device__ __forceinline__ long long grp_total_tiles(const GroupedArgs& p) {
+  const int lane = (int)(threadIdx.x & 31);
+  long long cnt = 0;
+  for (int g0 = 0; g0 < p.G; g0 += 32) {
+    const int g = g0 + lane;
+    if (g < p.G) {
+      int a = __ldg(p.offsets + g);
+      int b = __ldg(p.offsets + g + 1);
+      a = min(max(a, 0), p.M_total);
+      b = min(max(b, a), p.M_total);
+      cnt += (b - a + kGrpTileT - 1) / kGrpTileT;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  return cnt * p.n_tiles;
+}
+
 static __device__ __noinline__ void grouped_check_offsets(const GroupedArgs& p) {
   bool bad = __ldg(p.offsets) != 0 || __ldg(p.offsets + p.G) != p.M_total;
   int prev = 0;
@@ -148,7 +174,7 @@ static __device__ __noinline__ void grouped_check_offsets(const GroupedArgs& p) 
 
 __device__ __forceinline__ float grp_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
-template <bool OUT_F32, int EPI>
+template <bool OUT_F32, int EPI, bool CLC>
 __global__ void __launch_bounds__(kGrpThreads, 1)
     k_grouped_ws(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const GroupedArgs p) {
@@ -160,10 +186,14 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   uint8_t* smStg = smX + kGrpStages * kGrpXBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smStg + kGrpEpiWarps * kGrpStgBytes);
   // bars: full[S] | empty[S] | acc_full[2] | acc_empty[2] | tq_full[TQ] | tq_empty[TQ]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 4 + 2 * kGrpTQ);
+  //       | clc_full | clc_empty; then the 16-byte cancel response
+  constexpr int kNumBars = 2 * kGrpStages + 4 + 2 * kGrpTQ + 2;
+  static_assert(kNumBars % 2 == 0, "16-byte aligned response");
+  uint8_t* clc_resp = reinterpret_cast<uint8_t*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 16);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile int* tq_id = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [kGrpTQ]
-  static_assert((2 * kGrpStages + 4 + 2 * kGrpTQ) * 8 + (2 + kGrpTQ) * 4 <= 512, "barrier area");
+  static_assert(kNumBars * 8 + 16 + (2 + kGrpTQ) * 4 <= 512, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
@@ -174,9 +204,20 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   auto acce_bar = [&](int a) { return bar_base + 8u * (2 * kGrpStages + 2 + a); };
   auto tqf_bar = [&](int i) { return bar_base + 8u * (2 * kGrpStages + 4 + i); };
   auto tqe_bar = [&](int i) { return bar_base + 8u * (2 * kGrpStages + 4 + kGrpTQ + i); };
+  const uint32_t clcf_bar = bar_base + 8u * (kNumBars - 2);
+  const uint32_t clce_bar = bar_base + 8u * (kNumBars - 1);
   const uint32_t rank = cluster_ctarank();
   const long long cluster_id = blockIdx.x / 2;
   const long long num_clusters = gridDim.x / 2;
+
+  if constexpr (CLC) {
+    // A pair launched past the last tile has nothing to do (both CTAs of the
+    // pair reach the same verdict, before any cluster-wide step).
+    if (cluster_id >= grp_total_tiles(p)) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) grouped_check_offsets(p);
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGrpStages; ++s) {
@@ -187,12 +228,15 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), 2 * kGrpEpiWarps);
     }
-    // tile queue: filled by the leader's scheduler; emptied by every consumer
-    // of the pair (producer x2, epilogue warps x2*4, the leader's MMA issuer)
+    // Tile queue (cluster launch control): filled by this CTA's scheduler
+    // lane, emptied by this CTA's producer, epilogue warps and (leader) MMA
+    // issuer.  The cancel response is released by both CTAs' schedulers.
     for (int i = 0; i < kGrpTQ; ++i) {
       mbar_init(tqf_bar(i), 1);
-      mbar_init(tqe_bar(i), 2 + 2 * kGrpEpiWarps + 1);
+      mbar_init(tqe_bar(i), 1 + kGrpEpiWarps + (rank == 0 ? 1 : 0));
     }
+    mbar_init(clcf_bar, 1);
+    mbar_init(clce_bar, 2);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
@@ -209,19 +253,23 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const Guard guard{p.ws, abort_flag, p.timeout_ns};
 
-  // Next tile index for one consuming thread (dynamic schedule); false at
-  // the end of the work or when the CTA is aborting.  Every consumer reads
-  // every queue entry, including the final end marker.
-  auto take_tile = [&](int& slot, uint32_t& ph, long long& t) -> bool {
-    const bool got = rank == 0 ? wait_phase(guard, tqf_bar(slot), ph, (kRoleProducer << 16) | 0x500 | slot)
-                               : wait_phase_cluster(guard, tqf_bar(slot), ph, (kRoleProducer << 16) | 0x500 | slot);
-    if (!got) return false;
-    const int id = tq_id[slot];
-    if (rank == 0) mbar_arrive(tqe_bar(slot));
-    else mbar_arrive_cluster(map_to_cta(tqe_bar(slot), 0));
-    if (++slot == kGrpTQ) { slot = 0; ph ^= 1u; }
-    t = id;
-    return id >= 0;
+  // Next tile index for one consuming thread.  Static: the pair's own
+  // sequence.  Cluster launch control: the next entry of this CTA's tile
+  // queue (false at the end marker or when the CTA is aborting; every
+  // consumer reads every entry, including the end marker).
+  auto next_tile = [&](long long& t, bool& first, int& slot, uint32_t& ph) -> bool {
+    if constexpr (!CLC) {
+      t = first ? cluster_id : t + num_clusters;
+      first = false;
+      return true;
+    } else {
+      if (!wait_phase(guard, tqf_bar(slot), ph, (kRoleProducer << 16) | 0x500 | slot)) return false;
+      const int id = tq_id[slot];
+      mbar_arrive(tqe_bar(slot));
+      if (++slot == kGrpTQ) { slot = 0; ph ^= 1u; }
+      t = id;
+      return id >= 0;
+    }
   };
 
   if (warp == 0) {
@@ -232,14 +280,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       bool ok = true;
       GrpWalker gw;
       gw.init(p);
-#if GRP_DYNAMIC
       int tqs = 0;
       uint32_t tqph = 0;
       long long t = 0;
-      while (ok && take_tile(tqs, tqph, t) && gw.seek(p, t)) {
-#else
-      for (long long t = cluster_id; ok && gw.seek(p, t); t += num_clusters) {
-#endif
+      bool first = true;
+      while (ok && next_tile(t, first, tqs, tqph) && gw.seek(p, t)) {
         const GrpTile tl = gw.tile(p, t);
         const int w_row = tl.n0 + (int)rank * 128;
         const int x_row = tl.t0 + (int)rank * (tl.nmma >> 1);
@@ -276,14 +321,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       bool ok = true;
       GrpWalker gw;
       gw.init(p);
-#if GRP_DYNAMIC
       int tqs = 0;
       uint32_t tqph = 0;
       long long t = 0;
-      while (ok && take_tile(tqs, tqph, t) && gw.seek(p, t)) {
-#else
-      for (long long t = cluster_id; ok && gw.seek(p, t); t += num_clusters) {
-#endif
+      bool first = true;
+      while (ok && next_tile(t, first, tqs, tqph) && gw.seek(p, t)) {
         const GrpTile tl = gw.tile(p, t);
         const uint32_t idesc = idesc_bf16_f32(kGrpTileN, tl.nmma, false, false);
         if (!wait_phase_cluster(guard, acce_bar(acc), acc_phase ^ 1u, (kRoleMma << 16) | 0x100 | acc)) break;
@@ -315,26 +357,45 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     // Lane 1: validate the device offsets off the producers' critical path
     // (one pass, latches WST_ERR_BAD_OFFSETS).
     if (lane == 1 && blockIdx.x == 0) grouped_check_offsets(p);
-#if GRP_DYNAMIC
-    // Lane 0 of the leader: the pair's tile scheduler.
-    if (lane == 0 && rank == 0) {
-      GrpWalker sw;
-      sw.init(p);
-      int slot = 0;
-      uint32_t ph = 0;
-      while (true) {
-        if (!wait_phase_cluster(guard, tqe_bar(slot), ph ^ 1u, (kRoleProducer << 16) | 0x600 | slot)) break;
-        const uint32_t t = atomicAdd(&p.ws->sched_next, 1u);
-        const int id = sw.seek(p, (long long)t) ? (int)t : -1;
-        tq_id[slot] = id;
-        st_shared_cluster_u32(map_to_cta(smem_addr((const void*)(tq_id + slot)), 1), (uint32_t)id);
-        mbar_arrive(tqf_bar(slot));
-        mbar_arrive_cluster(map_to_cta(tqf_bar(slot), 1));
-        if (id < 0) break;
-        if (++slot == kGrpTQ) { slot = 0; ph ^= 1u; }
+    if constexpr (CLC) {
+      // Lane 0 (both CTAs): the tile scheduler.  The leader issues the cancel
+      // requests; both CTAs receive each response and queue the same tiles.
+      if (lane == 0) {
+        const uint32_t resp = smem_addr(clc_resp);
+        int slot = 0;
+        uint32_t ph = 0, cph = 0;
+        auto push = [&](int id) -> bool {
+          if (!wait_phase(guard, tqe_bar(slot), ph ^ 1u, (kRoleProducer << 16) | 0x600 | slot)) return false;
+          tq_id[slot] = id;
+          mbar_arrive(tqf_bar(slot));
+          if (++slot == kGrpTQ) { slot = 0; ph ^= 1u; }
+          return true;
+        };
+        GrpWalker sw;
+        sw.init(p);
+        bool ok = push((int)cluster_id);
+        while (ok) {
+          if (rank == 0) {
+            // Both schedulers have read the previous response.
+            if (!wait_phase_cluster(guard, clce_bar, cph ^ 1u, (kRoleProducer << 16) | 0x700)) break;
+            mbar_arrive_expect_tx(clcf_bar, 16);
+            clc_try_cancel_all(resp, clcf_bar);
+          } else {
+            mbar_arrive_expect_tx(clcf_bar, 16);
+          }
+          if (!wait_phase(guard, clcf_bar, cph, (kRoleProducer << 16) | 0x701)) break;
+          uint32_t first_x = 0;
+          const bool got = clc_query(resp, first_x);
+          if (rank == 0) mbar_arrive(clce_bar);
+          else mbar_arrive_cluster(map_to_cta(clce_bar, 0));
+          cph ^= 1u;
+          const long long t = (long long)(first_x >> 1);
+          if (!got || !sw.seek(p, t)) break;
+          ok = push((int)t);
+        }
+        if (ok) push(-1);
       }
     }
-#endif
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -344,19 +405,16 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     uint32_t acc_phase = 0;
     GrpWalker gw;
     gw.init(p);
-#if GRP_DYNAMIC
     int tqs = 0;
     uint32_t tqph = 0;
+    long long t = 0;
+    bool first = true;
     while (true) {
-      long long t = 0;
       uint32_t got = 0;
-      if (lane == 0) got = take_tile(tqs, tqph, t) ? 1u : 0u;
+      if (lane == 0) got = next_tile(t, first, tqs, tqph) ? 1u : 0u;
       got = __shfl_sync(0xffffffffu, got, 0);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (!got || !gw.seek(p, t)) break;
-#else
-    for (long long t = cluster_id; gw.seek(p, t); t += num_clusters) {
-#endif
       const GrpTile tl = gw.tile(p, t);
       if (!warp_wait_phase_cluster(guard, accf_bar(acc), acc_phase, (kRoleEpilogue << 16) | acc)) break;
       tc_fence_after_sync();
@@ -442,18 +500,6 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   cluster_sync();
   tc_fence_after_sync();
   if (warp == 2) tmem_dealloc<2>(tmem_base, 512);
-#if GRP_DYNAMIC
-  if (threadIdx.x == 0) {
-    // The last CTA to finish resets the tile counter for the next call.
-    __threadfence();
-    const uint32_t prev = atomicAdd(&p.ws->sched_done, 1u);
-    if (prev == gridDim.x - 1) {
-      p.ws->sched_next = 0u;
-      p.ws->sched_done = 0u;
-      __threadfence();
-    }
-  }
-#endif
 }
 
 }  // namespace wst

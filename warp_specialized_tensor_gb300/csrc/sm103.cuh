@@ -115,6 +115,39 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // ---------------------------------------------------------------------------
+// Cluster launch control (hardware work stealing, sm_100 and later)
+// ---------------------------------------------------------------------------
+// Asks the hardware to cancel the launch of one not-yet-started cluster of
+// this grid.  The 16-byte response is written at shared::cta offset `resp`
+// in every CTA of the calling cluster, and completes 16 tx-bytes on the
+// mbarrier at offset `bar` in each of them.  Once a response has reported
+// failure, no further request may be issued.
+__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+      ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Decodes a response: true, with the x index of the cancelled cluster's
+// first CTA, if a cluster was cancelled; false once none is left.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& first_x) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  first_x = x;
+  return ok != 0;
+}
+
+// ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
@@ -346,11 +379,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-// Weak store to a shared::cluster address (own or peer CTA).
-__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr_cluster, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {

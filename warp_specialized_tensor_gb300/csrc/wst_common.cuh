@@ -20,9 +20,7 @@ struct WsHeader {
   uint32_t error_info;  // where it happened (role << 16 | detail)
   uint32_t epoch;       // IKBO: flag value published by the last completed call
   uint32_t done_ctas;   // IKBO: CTAs of the running call that have finished
-  uint32_t sched_next;  // grouped: next tile index handed out by the dynamic scheduler
-  uint32_t sched_done;  // grouped: CTAs of the running call that have finished
-  uint32_t pad[58];
+  uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
