@@ -1,4 +1,4 @@
-"""CPU oracle for the three contractions (fp64 accumulation).
+"""CPU oracle for the hot path's contractions and IKBO attention (fp64).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 the benchmark's CPU-baseline / reference legs may import this package.  The
@@ -66,6 +66,12 @@ def _load():
             lib.oracle_ikbo_decomposed.argtypes = [I, I, I, I, I, I, P, P, P,
                                                    P, P, P]
             lib.oracle_ikbo_decomposed.restype = I
+            lib.oracle_ikbo_attention.argtypes = [I, I, I, I, I, I, P, P, P, P,
+                                                  ctypes.c_double, P, P, I]
+            lib.oracle_ikbo_attention.restype = I
+            lib.oracle_ikbo_attention_grouped.argtypes = [I, I, I, I, I, I, P, P, P, P,
+                                                          ctypes.c_double, P]
+            lib.oracle_ikbo_attention_grouped.restype = I
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -235,3 +241,55 @@ def ikbo_decomposed(U, Cf, W, user_offsets) -> np.ndarray:
     if rc != 0:
         raise ValueError("bad user offsets")
     return Y
+
+
+def _attn_shapes(Q, K, V, user_offsets, Lq):
+    q = _u16(Q)
+    k = _u16(K)
+    v = _u16(V)
+    off = np.ascontiguousarray(np.asarray(user_offsets, dtype=np.int32))
+    nu, Lkv, H, Dh = k.shape
+    if v.shape != k.shape or off.size != nu + 1:
+        raise ValueError("shape mismatch")
+    nq, Hq, Dq = q.shape
+    if Hq != H or Dq != Dh or nq % Lq:
+        raise ValueError("query shape")
+    return q, k, v, off, nu, nq // Lq, Lkv, H, Dh
+
+
+def ikbo_attention(Q, K, V, user_offsets, Lq: int = 1, scale=None, cands=None) -> np.ndarray:
+    """IKBO attention, materialised form: each query row of candidate c
+    attends over its user's keys/values (one copy per candidate), per head.
+
+    Q [num_cand*Lq, H, Dh], K/V [users, Lkv, H, Dh] bf16; scale defaults to
+    1/sqrt(Dh).  Returns fp64 [num_cand*Lq, H, Dh] (rows of candidates not in
+    ``cands`` are NaN when ``cands`` is given)."""
+    lib = _load()
+    q, k, v, off, nu, nc, Lkv, H, Dh = _attn_shapes(Q, K, V, user_offsets, Lq)
+    if scale is None:
+        scale = 1.0 / np.sqrt(Dh)
+    O = np.full((nc * Lq, H, Dh), np.nan, dtype=np.float64)
+    cands_a, ncands = None, 0
+    if cands is not None:
+        cands_a = np.ascontiguousarray(np.asarray(cands, dtype=np.int32))
+        ncands = cands_a.size
+    rc = lib.oracle_ikbo_attention(nu, nc, Lq, H, Dh, Lkv, _ptr(q), _ptr(k), _ptr(v), _ptr(off),
+                                   float(scale), _ptr(O), _ptr(cands_a), ncands)
+    if rc != 0:
+        raise ValueError("bad user offsets or candidate index (rc=%d)" % rc)
+    return O
+
+
+def ikbo_attention_grouped(Q, K, V, user_offsets, Lq: int = 1, scale=None) -> np.ndarray:
+    """IKBO attention, second coding (per user: stacked queries, S = QK^T,
+    row softmax, O = PV).  Same conventions as ikbo_attention()."""
+    lib = _load()
+    q, k, v, off, nu, nc, Lkv, H, Dh = _attn_shapes(Q, K, V, user_offsets, Lq)
+    if scale is None:
+        scale = 1.0 / np.sqrt(Dh)
+    O = np.full((nc * Lq, H, Dh), np.nan, dtype=np.float64)
+    rc = lib.oracle_ikbo_attention_grouped(nu, nc, Lq, H, Dh, Lkv, _ptr(q), _ptr(k), _ptr(v),
+                                           _ptr(off), float(scale), _ptr(O))
+    if rc != 0:
+        raise ValueError("bad user offsets (rc=%d)" % rc)
+    return O

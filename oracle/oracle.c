@@ -1,7 +1,8 @@
 /*
- * oracle.c -- plain, slow, obviously correct CPU oracle for the three
- * contractions of the hot path.  TEST INFRASTRUCTURE ONLY: the product path
- * (the CUDA library) never links, loads or calls this file; only the tests,
+ * oracle.c -- plain, slow, obviously correct CPU oracle for the
+ * contractions of the hot path and for IKBO attention.  TEST
+ * INFRASTRUCTURE ONLY: the product path (the CUDA library) never links,
+ * loads or calls this file; only the tests,
  * the smoke check and the benchmark's CPU-baseline leg do.
  *
  * Everything is accumulated in IEEE double.  bf16 inputs (passed as their
@@ -32,6 +33,19 @@
  *                column-wise into the user part and the candidate part,
  *                Y[c] = W_u . U[u] + W_c . C[c].  A second, independent
  *                coding used only to cross-check the materialised form.
+ *   ikbo_attention -- [P1] "Case Study 2" names an IKBO form of
+ *                FlashAttention in which the candidates of one user share
+ *                the reads of that user's keys and values.  The pages print
+ *                no formula; the reading used: every query row of candidate
+ *                c attends over the
+ *                context (keys, values) of its user u = user(c), per head,
+ *                o = sum_j softmax_j(scale * q . k_j) v_j, no mask.  The
+ *                reference form materialises the broadcast: one copy of the
+ *                user's K and V per candidate.
+ *   ikbo_attention_grouped -- a second coding of the same result: per user
+ *                and head, the query rows of all of the user's candidates
+ *                stacked into one matrix, S = Q K^T, row softmax, O = P V
+ *                (the IKBO form), with no per-candidate copy.
  *
  * Threading: OpenMP over independent output rows / candidates only; each
  * output element is one sequential k-ordered sum, so the thread count does
@@ -282,4 +296,131 @@ int oracle_ikbo_decomposed(int num_users, int num_cand, int Du, int Dc, int D, i
             }
     }
     return 0;
+}
+
+/*
+ * IKBO attention, materialised reference form.
+ *   Q : bf16 [num_cand*Lq][H][Dh]      query rows; candidate c owns rows
+ *                                      [c*Lq, (c+1)*Lq)
+ *   K, V: bf16 [num_users][Lkv][H][Dh] each user's context
+ *   uoff: host int[num_users+1], candidates of user u are [uoff[u], uoff[u+1])
+ *   scale: logit scale
+ *   Out : double [num_cand*Lq][H][Dh]
+ *   cands: if non-NULL, only the listed candidates (ncands) are computed.
+ * For each candidate and head the user's keys and values are copied out (the
+ * broadcast the in-kernel method avoids); each query row q of the candidate
+ * then takes s_j = scale * q . k_j over the copy, p_j = exp(s_j - max s) /
+ * sum_i exp(s_i - max s), and o = sum_j p_j v_j.  Returns -1 on bad offsets,
+ * -2 on a bad candidate index or allocation failure.
+ */
+int oracle_ikbo_attention(int num_users, int num_cand, int Lq, int H, int Dh, int Lkv,
+                          const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                          const int *uoff, double scale, double *Out,
+                          const int *cands, int ncands)
+{
+    if (uoff[0] != 0 || uoff[num_users] != num_cand) return -1;
+    for (int u = 0; u < num_users; ++u)
+        if (uoff[u + 1] < uoff[u]) return -1;
+    long n = cands ? ncands : num_cand;
+    int bad = 0;
+    #pragma omp parallel
+    {
+        double *Kc = (double *)malloc(sizeof(double) * (size_t)Lkv * (size_t)Dh);
+        double *Vc = (double *)malloc(sizeof(double) * (size_t)Lkv * (size_t)Dh);
+        double *sc = (double *)malloc(sizeof(double) * (size_t)Lkv);
+        if (!Kc || !Vc || !sc) bad = 1;
+        #pragma omp for schedule(dynamic, 1) collapse(2)
+        for (long i = 0; i < n; ++i)
+            for (int h = 0; h < H; ++h) {
+                int c = cands ? cands[i] : (int)i;
+                if (!Kc || !Vc || !sc || c < 0 || c >= num_cand) { bad = 1; continue; }
+                int u = user_of(num_users, uoff, c);
+                /* The broadcast: this candidate's own copy of K[u], V[u] (head h). */
+                for (int j = 0; j < Lkv; ++j)
+                    for (int d = 0; d < Dh; ++d) {
+                        long src = (((long)u * Lkv + j) * H + h) * Dh + d;
+                        Kc[(long)j * Dh + d] = bf16_to_double(K[src]);
+                        Vc[(long)j * Dh + d] = bf16_to_double(V[src]);
+                    }
+                for (int r = 0; r < Lq; ++r) {
+                    long row = (long)c * Lq + r;
+                    const uint16_t *q = Q + (row * H + h) * Dh;
+                    double mx = -INFINITY;
+                    for (int j = 0; j < Lkv; ++j) {
+                        double acc = 0.0;
+                        for (int d = 0; d < Dh; ++d)
+                            acc += bf16_to_double(q[d]) * Kc[(long)j * Dh + d];
+                        sc[j] = scale * acc;
+                        if (sc[j] > mx) mx = sc[j];
+                    }
+                    double sum = 0.0;
+                    for (int j = 0; j < Lkv; ++j) {
+                        sc[j] = exp(sc[j] - mx);
+                        sum += sc[j];
+                    }
+                    double *o = Out + (row * H + h) * Dh;
+                    for (int d = 0; d < Dh; ++d) {
+                        double acc = 0.0;
+                        for (int j = 0; j < Lkv; ++j)
+                            acc += sc[j] * Vc[(long)j * Dh + d];
+                        o[d] = acc / sum;
+                    }
+                }
+            }
+        free(Kc);
+        free(Vc);
+        free(sc);
+    }
+    return bad ? -2 : 0;
+}
+
+/*
+ * IKBO attention, second coding: per user u and head h, the rows of all of
+ * u's candidates form one matrix Qs [nq][Dh]; S = scale * Qs K[u]^T, each row
+ * of S is normalised (P = exp(S - rowmax) / rowsum), and O = P V[u].  Same
+ * conventions as oracle_ikbo_attention (all candidates).
+ */
+int oracle_ikbo_attention_grouped(int num_users, int num_cand, int Lq, int H, int Dh, int Lkv,
+                                  const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                  const int *uoff, double scale, double *Out)
+{
+    if (uoff[0] != 0 || uoff[num_users] != num_cand) return -1;
+    for (int u = 0; u < num_users; ++u)
+        if (uoff[u + 1] < uoff[u]) return -1;
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int u = 0; u < num_users; ++u)
+        for (int h = 0; h < H; ++h) {
+            long r0 = (long)uoff[u] * Lq, nq = (long)(uoff[u + 1] - uoff[u]) * Lq;
+            if (nq == 0) continue;
+            double *P = (double *)malloc(sizeof(double) * (size_t)nq * (size_t)Lkv);
+            if (!P) { bad = 1; continue; }
+            for (long r = 0; r < nq; ++r) {
+                double mx = -INFINITY;
+                for (int j = 0; j < Lkv; ++j) {
+                    double acc = 0.0;
+                    for (int d = 0; d < Dh; ++d)
+                        acc += bf16_to_double(Q[((r0 + r) * H + h) * Dh + d]) *
+                               bf16_to_double(K[(((long)u * Lkv + j) * H + h) * Dh + d]);
+                    P[r * Lkv + j] = scale * acc;
+                    if (P[r * Lkv + j] > mx) mx = P[r * Lkv + j];
+                }
+                double sum = 0.0;
+                for (int j = 0; j < Lkv; ++j) {
+                    P[r * Lkv + j] = exp(P[r * Lkv + j] - mx);
+                    sum += P[r * Lkv + j];
+                }
+                for (int j = 0; j < Lkv; ++j) P[r * Lkv + j] /= sum;
+            }
+            for (long r = 0; r < nq; ++r)
+                for (int d = 0; d < Dh; ++d) {
+                    double acc = 0.0;
+                    for (int j = 0; j < Lkv; ++j)
+                        acc += P[r * Lkv + j] *
+                               bf16_to_double(V[(((long)u * Lkv + j) * H + h) * Dh + d]);
+                    Out[((r0 + r) * H + h) * Dh + d] = acc;
+                }
+            free(P);
+        }
+    return bad ? -2 : 0;
 }

@@ -135,7 +135,29 @@ def ikbo(users: int = 64, cand_per_user=128, Du: int = 256, Dc: int = 64,
     return {"U": U, "C": C, "W": W, "user_offsets": offsets}
 
 
-# The five named workloads at full size.
+def ikbo_attention(users: int = 32, cand_per_user=256, Lq: int = 2, H: int = 4,
+                   Dh: int = 128, Lkv: int = 2048, seed: int = SEED_BASE + 5):
+    """IKBO attention inputs: every query row of a candidate attends over its
+    user's context.
+
+    Q [num_cand*Lq, H, Dh] (candidate c owns rows [c*Lq, (c+1)*Lq)), K and V
+    [users, Lkv, H, Dh], all N(0, 1) in bf16; user_offsets int32 [users+1]
+    over candidates (cand_per_user: an int or a list of counts, zeros
+    allowed)."""
+    g = _gen(seed)
+    counts = [cand_per_user] * users if isinstance(cand_per_user, int) else list(cand_per_user)
+    if len(counts) != users:
+        raise ValueError("cand_per_user")
+    offsets = torch.zeros(users + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int64), 0).to(torch.int32)
+    ncand = int(offsets[-1])
+    Q = _normal(g, (ncand * Lq, H, Dh), 1.0)
+    K = _normal(g, (users, Lkv, H, Dh), 1.0)
+    V = _normal(g, (users, Lkv, H, Dh), 1.0)
+    return {"Q": Q, "K": K, "V": V, "user_offsets": offsets, "Lq": Lq}
+
+
+# The named workloads at full size.
 def workload(name: str):
     if name == "dense256":
         return dense(256, 256, 256, seed=SEED_BASE + 0, dist="uniform")
@@ -147,7 +169,9 @@ def workload(name: str):
         return ikbo(seed=SEED_BASE + 3)
     if name == "skinny_batch":
         return dense(1024, 256, 512, batch=512, seed=SEED_BASE + 4, bias=True)
+    if name == "ikbo_attention":
+        return ikbo_attention(seed=SEED_BASE + 5)
     raise KeyError(name)
 
 
-WORKLOADS = ("dense256", "dense8192", "grouped_moe", "ikbo", "skinny_batch")
+WORKLOADS = ("dense256", "dense8192", "grouped_moe", "ikbo", "skinny_batch", "ikbo_attention")
