@@ -206,6 +206,36 @@ wst_status wst_ikbo_linear_compress_noalloc(int num_users, int num_cand, int Du,
                                             const int* d_user_offsets, void* Y,
                                             int* d_status, void* stream);
 
+/*
+ * IKBO attention ("How We Built TLX: A Hardware-Native GPU Compiler for
+ * Production ML at Scale", Case Study 2, which names an IKBO form of
+ * FlashAttention whose key/value reads are shared by the candidates of one
+ * user; the pages give no formula, and the reading implemented is below).
+ * Candidates of user u are [off[u], off[u+1]) of the DEVICE int32 array
+ * d_user_offsets (num_users+1 entries, non-decreasing, from 0 to num_cand);
+ * candidate c owns the Lq query rows [c*Lq, (c+1)*Lq).  For every query row r
+ * of a candidate of user u and every head h:
+ *   O[r][h][:] = sum_j softmax_j(scale * Q[r][h][:] . K[u][j][h][:]) V[u][j][h][:]
+ * over all Lkv context rows j of user u (no mask).
+ *   Q   bf16 [num_cand*Lq][H][Dh]    (Dh contiguous)
+ *   K   bf16 [num_users][Lkv][H][Dh]
+ *   V   bf16 [num_users][Lkv][H][Dh]
+ *   O   o_type [num_cand*Lq][H][Dh]  (fp32 or bf16)
+ *   scale  any finite float (1/sqrt(Dh) is the usual choice)
+ * The query rows of all candidates of a user are processed together in
+ * 128-row tiles, so each user's K/V is read once per tile and per head, not
+ * once per candidate.  The probabilities are rounded to bf16 before the
+ * product with V; row maxima, sums and the output accumulate in fp32.
+ * This build supports Dh == 128 (else WST_ERR_UNSUPPORTED) and needs
+ * num_cand*Lq < 2^31.  `workspace` needs wst_workspace_size(0, 0, 0) bytes
+ * (the error word).  Offsets that break the rule are clamped into range on
+ * the device and latched as WST_ERR_BAD_OFFSETS.
+ */
+wst_status wst_ikbo_attention_bf16(int num_users, int num_cand, int Lq, int H, int Dh, int Lkv,
+                                   const void* Q, const void* K, const void* V,
+                                   const int* d_user_offsets, float scale,
+                                   void* O, wst_dtype o_type, void* workspace, void* stream);
+
 /* Synchronize `stream`, then return and clear the first device-side error
  * latched in `workspace` (WST_OK if none). */
 wst_status wst_sync_status(void* workspace, void* stream);

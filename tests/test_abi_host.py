@@ -94,3 +94,29 @@ def test_grouped_and_ikbo_reject(lib):
     assert k(*bad) == wst.WST_ERR_INVALID_ARG
     bad = list(args); bad[6] = FAKE + 4
     assert k(*bad) == wst.WST_ERR_ALIGNMENT
+
+
+def test_ikbo_attention_rejects(lib):
+    a = lib.wst_ikbo_attention_bf16
+    #       users cand Lq H  Dh   Lkv  Q     K     V     off   scale O     type ws    stream
+    args = [32, 8192, 2, 4, 128, 2048, FAKE, FAKE, FAKE, FAKE, 0.088, FAKE, 1, FAKE, None]
+    bad = list(args); bad[4] = 64            # Dh != 128
+    assert a(*bad) == wst.WST_ERR_UNSUPPORTED
+    bad = list(args); bad[5] = 0             # empty context
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[2] = 0             # no query rows per candidate
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[10] = float("nan")
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[10] = float("inf")
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[12] = 7            # unknown output type
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[1] = 1 << 30; bad[2] = 4   # 2^32 query rows
+    assert a(*bad) == wst.WST_ERR_UNSUPPORTED
+    bad = list(args); bad[7] = FAKE + 8      # K not 16-byte aligned
+    assert a(*bad) == wst.WST_ERR_ALIGNMENT
+    bad = list(args); bad[9] = FAKE + 2      # offsets not 4-byte aligned
+    assert a(*bad) == wst.WST_ERR_ALIGNMENT
+    bad = list(args); bad[11] = None
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG

@@ -1,0 +1,107 @@
+"""GPU parity: IKBO attention (candidate queries over their user's context)
+against the fp64 oracle.
+
+Tolerance, from the kernel's arithmetic: the probabilities are rounded to
+bf16 (relative error <= 2^-9) before the product with V, while the row sums,
+maxima and the output accumulate in fp32, so |O_gpu - O_ref| <= 2^-9 max|V|
+plus fp32 rounding.  The test allows 2^-8 max|V| (a factor 2 of margin),
+plus one bf16 ulp of the reference for bf16 outputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from oracle import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wst():
+    import warp_specialized_tensor_gb300 as w
+    w.load_library()
+    return w
+
+
+def run(wst, d, out_dtype=torch.float32, scale=None):
+    Q, K, V, off = d["Q"].cuda(), d["K"].cuda(), d["V"].cuda(), d["user_offsets"].cuda()
+    O = torch.full(Q.shape, float("nan"), dtype=out_dtype, device="cuda")
+    ws = wst.workspace()
+    wst.wst_ikbo_attention_bf16(Q, K, V, off, O, Lq=d["Lq"], scale=scale, workspace=ws)
+    return O, wst.wst_sync_status(ws)
+
+
+def check(O, ref, V, out_bf16, rows=None, what=""):
+    g = O.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        g, ref = g[rows], ref[rows]
+    assert not np.isnan(ref).any()
+    tol = 2.0 ** -8 * float(V.float().abs().max())
+    bound = tol + (compare.ulp_bf16(ref) if out_bf16 else 0.0)
+    err = np.abs(g - ref)
+    bad = ~(err <= bound)
+    assert not bad.any(), "%s: %d elements out of tolerance, max err %.3g (tol %.3g) at %s" % (
+        what, int(bad.sum()), float(np.nanmax(err)), tol, np.argwhere(bad)[:3].tolist())
+    return float(err.max()) / tol
+
+
+@pytest.mark.parametrize("counts,Lq,H,Lkv", [
+    ([40, 0, 130, 7], 2, 2, 200),   # ragged users (one empty), 3 key blocks + 8
+    ([64], 2, 1, 64),               # exactly one query tile and one key block
+    ([1, 3, 2], 1, 3, 1),           # a single key: O = V[u, 0]
+    ([100, 28], 1, 2, 65),          # one key past a block edge
+    ([300], 3, 1, 130),             # 900 query rows of one user: 8 tiles
+])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_attention_parity(wst, counts, Lq, H, Lkv, out):
+    d = synthetic.ikbo_attention(users=len(counts), cand_per_user=counts, Lq=Lq, H=H, Lkv=Lkv,
+                                 seed=len(counts) * 100 + Lkv)
+    O, st = run(wst, d, out)
+    assert st == 0
+    ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], Lq)
+    check(O, ref, d["V"], out == torch.bfloat16, what="attention %s" % (counts,))
+
+
+def test_attention_single_key_is_exact_value(wst):
+    d = synthetic.ikbo_attention(users=2, cand_per_user=[5, 9], Lq=2, H=2, Lkv=1, seed=3)
+    O, st = run(wst, d, torch.float32)
+    assert st == 0
+    users = np.repeat([0, 1], np.array([5, 9]) * 2)
+    want = d["V"].float()[users, 0]
+    assert torch.equal(O.cpu(), want)
+
+
+def test_attention_scale_argument(wst):
+    d = synthetic.ikbo_attention(users=2, cand_per_user=[20, 30], Lq=1, H=2, Lkv=150, seed=4)
+    O, st = run(wst, d, torch.float32, scale=0.5)
+    assert st == 0
+    ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 1, scale=0.5)
+    check(O, ref, d["V"], False, what="scale 0.5")
+
+
+def test_attention_full_size_sampled(wst):
+    d = synthetic.workload("ikbo_attention")
+    O, st = run(wst, d, torch.bfloat16)
+    assert st == 0
+    off = d["user_offsets"].tolist()
+    Lq = d["Lq"]
+    g = torch.Generator().manual_seed(5)
+    cands = set()
+    for u in torch.randperm(len(off) - 1, generator=g)[:4].tolist():
+        cands |= {off[u], off[u + 1] - 1, (off[u] + off[u + 1]) // 2, min(off[u] + 64, off[u + 1] - 1)}
+    cands = sorted(cands)
+    ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], Lq, cands=cands)
+    rows = [c * Lq + r for c in cands for r in range(Lq)]
+    check(O, ref, d["V"], True, rows=rows, what="full size")
+    assert not torch.isnan(O.float()).any(), "unwritten rows"
+
+
+def test_attention_bad_offsets_latched(wst):
+    d = synthetic.ikbo_attention(users=3, cand_per_user=[10, 10, 10], Lq=1, H=1, Lkv=70, seed=6)
+    d["user_offsets"] = torch.tensor([0, 20, 5, 30], dtype=torch.int32)
+    O, st = run(wst, d)
+    assert st == wst.WST_ERR_BAD_OFFSETS

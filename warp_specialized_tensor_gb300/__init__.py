@@ -10,6 +10,7 @@ A non-OK status raises :class:`WstError`.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 
@@ -21,7 +22,8 @@ __all__ = [
     "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "F32", "BF16",
     "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
     "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_grouped_gemm_bf16",
-    "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_sync_status", "wst_status_string",
+    "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
+    "wst_sync_status", "wst_status_string",
     "wst_version",
 ]
 
@@ -74,6 +76,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_ikbo_linear_compress.restype = I
         lib.wst_ikbo_linear_compress_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
         lib.wst_ikbo_linear_compress_noalloc.restype = I
+        lib.wst_ikbo_attention_bf16.argtypes = [I, I, I, I, I, I, P, P, P, P, ctypes.c_float,
+                                                P, I, P, P]
+        lib.wst_ikbo_attention_bf16.restype = I
         lib.wst_sync_status.argtypes = [P, P]
         lib.wst_sync_status.restype = I
         lib.wst_status_string.argtypes = [I]
@@ -279,6 +284,39 @@ def wst_ikbo_linear_compress(U, Cf, W, user_offsets, Y, workspace, stream=None) 
         users, cand, Du, Dc, D, O, U.data_ptr(), Cf.data_ptr(), W.data_ptr(),
         user_offsets.data_ptr(), Y.data_ptr(), workspace.data_ptr(), _stream_handle(stream))
     _check(st, "wst_ikbo_linear_compress")
+
+
+def wst_ikbo_attention_bf16(Q, K, V, user_offsets, O, Lq: int = 1, scale=None, workspace=None,
+                            stream=None) -> None:
+    """IKBO attention: every query row of a candidate of user u attends over
+    u's context, per head: O[r][h] = softmax(scale * Q[r][h] . K[u][:, h]^T) V[u][:, h].
+
+    Q: bf16 [cand*Lq, H, Dh]; K, V: bf16 [users, Lkv, H, Dh];
+    user_offsets: device int32 [users+1] (candidates per user);
+    O: fp32 or bf16 [cand*Lq, H, Dh]; scale defaults to 1/sqrt(Dh)."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, torch.bfloat16, (3,) if n == "Q" else (4,))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    _need(user_offsets, "user_offsets", torch.int32, (1,))
+    if O.dtype not in (torch.float32, torch.bfloat16) or not O.is_contiguous():
+        raise ValueError("O must be a contiguous fp32 or bf16 tensor")
+    users, Lkv, H, Dh = K.shape
+    nq = Q.shape[0]
+    if V.shape != K.shape or Q.shape[1:] != (H, Dh) or O.shape != Q.shape or nq % Lq:
+        raise ValueError("shape mismatch")
+    if user_offsets.numel() != users + 1:
+        raise ValueError("user_offsets needs users+1 entries")
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dh)
+    if workspace is None:
+        raise ValueError("workspace is required")
+    st = load_library().wst_ikbo_attention_bf16(
+        users, nq // Lq, Lq, H, Dh, Lkv, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+        user_offsets.data_ptr(), float(scale), O.data_ptr(),
+        F32 if O.dtype == torch.float32 else BF16, workspace.data_ptr(),
+        _stream_handle(stream))
+    _check(st, "wst_ikbo_attention_bf16")
 
 
 def wst_ikbo_linear_compress_noalloc(U, Cf, W, user_offsets, Y, status=None,

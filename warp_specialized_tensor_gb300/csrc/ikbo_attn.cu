@@ -1,0 +1,79 @@
+// ikbo_attn.cu -- instantiations and launcher of the IKBO attention kernel:
+// tensor maps over Q and the users' K/V, kernel arguments, grid size, launch.
+#include <algorithm>
+
+#include "ikbo_attn_ws.cuh"
+#include "wst_host.h"
+
+namespace wst {
+
+namespace {
+
+template <bool OUT_F32>
+int launch_attn(const AttnProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
+  auto kern = k_ikbo_attn_ws<OUT_F32>;
+  int st;
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t nq = (uint64_t)pr.num_cand * (uint64_t)pr.Lq;
+  const uint64_t row_bytes = (uint64_t)pr.H * kAttnDh * 2;
+  {
+    // Q rows, one head at a time: {Dh, H, rows}, boxes of 64 d x 1 head x 128 rows
+    uint64_t dims[3] = {(uint64_t)kAttnDh, (uint64_t)pr.H, nq};
+    uint64_t str[2] = {(uint64_t)kAttnDh * 2, row_bytes};
+    uint32_t box[3] = {64, 1, (uint32_t)kAttnBM};
+    if ((st = encode_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pr.Q, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    // K and V: {Dh, H, Lkv, users}, boxes of 64 d x 1 head x 64 keys x 1 user;
+    // keys past Lkv read as zero (and are masked in the softmax)
+    uint64_t dims[4] = {(uint64_t)kAttnDh, (uint64_t)pr.H, (uint64_t)pr.Lkv, (uint64_t)pr.num_users};
+    uint64_t str[3] = {(uint64_t)kAttnDh * 2, row_bytes, row_bytes * (uint64_t)pr.Lkv};
+    uint32_t box[4] = {64, 1, (uint32_t)kAttnBN, 1};
+    if ((st = encode_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pr.K, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+    if ((st = encode_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pr.V, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  AttnArgs a{};
+  a.num_users = pr.num_users;
+  a.num_cand = pr.num_cand;
+  a.Lq = pr.Lq;
+  a.H = pr.H;
+  a.Lkv = pr.Lkv;
+  a.kv_blocks = (pr.Lkv + kAttnBN - 1) / kAttnBN;
+  a.scale_log2 = (float)((double)pr.scale * 1.4426950408889634);  // scale * log2(e)
+  a.uoff = pr.uoff;
+  a.O = pr.O;
+  a.ws = static_cast<WsHeader*>(pr.ws);
+  a.timeout_ns = wait_timeout_ns();
+
+  // Persistent grid: one CTA per SM, no more than the items can use (the
+  // per-user tile counts live on the device: bound them by H * (tiles + users)).
+  const long long items_max =
+      (long long)pr.H * ((long long)((nq + kAttnBM - 1) / kAttnBM) + pr.num_users);
+  const long long grid = std::max(1LL, std::min<long long>(dev.num_sms, items_max));
+  if ((st = ensure_smem_attr((const void*)kern, kAttnSmemBytes))) return st;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAttnSmemBytes;
+  cfg.stream = stream;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, a);
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_ikbo_attn_ws");
+  return ST_OK;
+}
+
+}  // namespace
+
+int run_ikbo_attention(const AttnProblem& pr, cudaStream_t stream) {
+  DeviceInfo dev;
+  int st = current_device_info(&dev);
+  if (st) return st;
+  return pr.o_f32 ? launch_attn<true>(pr, dev, stream) : launch_attn<false>(pr, dev, stream);
+}
+
+}  // namespace wst

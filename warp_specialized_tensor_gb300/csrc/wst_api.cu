@@ -376,6 +376,51 @@ wst_status wst_grouped_gemm_bf16(int G, int M_total, int N, int K, const void* A
   return (wst_status)run_gemm(p, static_cast<cudaStream_t>(stream));
 }
 
+wst_status wst_ikbo_attention_bf16(int num_users, int num_cand, int Lq, int H, int Dh, int Lkv,
+                                   const void* Q, const void* K, const void* V,
+                                   const int* d_user_offsets, float scale, void* O,
+                                   wst_dtype o_type, void* workspace, void* stream) {
+  g_err[0] = 0;
+  if (num_users < 1 || num_cand < 0 || Lq < 1 || H < 1 || Dh < 1 || Lkv < 1)
+    return fail(WST_ERR_INVALID_ARG, "sizes out of range (users=%d cand=%d Lq=%d H=%d Dh=%d Lkv=%d)",
+                num_users, num_cand, Lq, H, Dh, Lkv);
+  if (o_type != WST_F32 && o_type != WST_BF16) return fail(WST_ERR_INVALID_ARG, "unknown o_type %d", (int)o_type);
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+    return fail(WST_ERR_INVALID_ARG, "scale must be finite");
+  if (!Q || !K || !V || !d_user_offsets || !O || !workspace)
+    return fail(WST_ERR_INVALID_ARG, "Q, K, V, offsets, O and workspace must be non-NULL");
+  if (Dh != 128) return fail(WST_ERR_UNSUPPORTED, "Dh=%d: this build supports Dh == 128", Dh);
+  if ((long long)num_cand * Lq > 0x7fffffffLL)
+    return fail(WST_ERR_UNSUPPORTED, "num_cand*Lq = %lld query rows: needs < 2^31", (long long)num_cand * Lq);
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(d_user_offsets) & 3u))
+    return fail(WST_ERR_ALIGNMENT, "Q, K, V, O, workspace must be 16-byte aligned, offsets 4-byte");
+  WST_TRY(check_device_ptr(Q, "Q"));
+  WST_TRY(check_device_ptr(K, "K"));
+  WST_TRY(check_device_ptr(V, "V"));
+  WST_TRY(check_device_ptr(O, "O"));
+  WST_TRY(check_device_ptr(d_user_offsets, "d_user_offsets"));
+  WST_TRY(check_device_ptr(workspace, "workspace"));
+  if (num_cand == 0) return WST_OK;  // no query rows: nothing to output
+
+  AttnProblem p{};
+  p.num_users = num_users;
+  p.num_cand = num_cand;
+  p.Lq = Lq;
+  p.H = H;
+  p.Dh = Dh;
+  p.Lkv = Lkv;
+  p.Q = Q;
+  p.K = K;
+  p.V = V;
+  p.uoff = d_user_offsets;
+  p.scale = scale;
+  p.O = O;
+  p.o_f32 = o_type == WST_F32;
+  p.ws = workspace;
+  return (wst_status)run_ikbo_attention(p, static_cast<cudaStream_t>(stream));
+}
+
 wst_status wst_ikbo_linear_compress(int num_users, int num_cand, int Du, int Dc, int D, int O,
                                     const void* U, const void* Cf, const void* W,
                                     const int* d_user_offsets, void* Y, void* workspace,

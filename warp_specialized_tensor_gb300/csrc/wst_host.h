@@ -82,7 +82,22 @@ struct IkboProblem {
   void* ws;
 };
 
+// IKBO attention: Q [num_cand*Lq][H][Dh], K/V [num_users][Lkv][H][Dh] (bf16),
+// O [num_cand*Lq][H][Dh] (fp32 or bf16).
+struct AttnProblem {
+  int num_users, num_cand, Lq, H, Dh, Lkv;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const int* uoff;
+  float scale;
+  void* O;
+  bool o_f32;
+  void* ws;
+};
+
 int run_gemm(const GemmProblem& p, cudaStream_t stream);
+int run_ikbo_attention(const AttnProblem& p, cudaStream_t stream);
 int run_ikbo(const IkboProblem& p, cudaStream_t stream);
 int run_ikbo_noalloc(IkboProblem p, int* d_status, cudaStream_t stream);
 size_t ikbo_noalloc_capacity();
