@@ -411,8 +411,8 @@ def run_ours(args, rank, world, dist):
 
 def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20):
     """dense 256^3 (fp32 out; launch-latency bound), the skinny recsys batch
-    (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2), and the
-    row-RMSNorm-fused GEMM on the dense 8192^3 operands."""
+    (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2), the
+    row-RMSNorm-fused GEMM on the dense 8192^3 operands, and IKBO attention."""
     import synthetic
     out = {}
     cases = []
@@ -436,6 +436,20 @@ def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20):
     cases.append(("dense8192_rmsnorm",
                   lambda: wst.wst_gemm_rmsnorm_bf16(A2, B2, C2, eps=1e-6, workspace=ws, stream=stream),
                   dense_flops(8192, 8192, 8192), dense_bytes(8192, 8192, 8192)))
+    # IKBO attention: 32 users x 256 candidates x 2 query rows, 4 heads, Dh 128,
+    # 2048 context rows per user; bf16 out.  FLOPs: QK^T and PV; bytes: Q, the
+    # users' K and V once, O.
+    d6 = synthetic.workload("ikbo_attention")
+    Q6, K6, V6 = d6["Q"].to(dev), d6["K"].to(dev), d6["V"].to(dev)
+    off6 = d6["user_offsets"].to(dev)
+    O6 = torch.empty(Q6.shape, dtype=torch.bfloat16, device=dev)
+    nq6, H6, Dh6 = Q6.shape
+    Lkv6 = K6.shape[1]
+    cases.append(("ikbo_attention",
+                  lambda: wst.wst_ikbo_attention_bf16(Q6, K6, V6, off6, O6, Lq=d6["Lq"],
+                                                      workspace=ws, stream=stream),
+                  4.0 * nq6 * Lkv6 * Dh6 * H6,
+                  2 * (2 * nq6 * H6 * Dh6) + 2 * (2 * K6.numel())))
     for name, fn, fl, by in cases:
         for _ in range(3):
             fn()

@@ -13,25 +13,30 @@
 //     O[r][h] = sum_j softmax_j(scale * Q[r][h] . K[u][j][h]) * V[u][j][h]
 //
 // In-kernel broadcast: the query rows of ALL candidates of user u are stacked
-// into 128-row tiles, and every tile streams K[u][:, h] and V[u][:, h] once.
-// The context is then read once per 128 query rows instead of once per
-// candidate.  Work item = (user u, head h, query tile t), with t fastest so the
-// tiles that share a context run side by side and hit L2.  Persistent CTAs
-// take items blockIdx.x, blockIdx.x + gridDim.x, ...
+// and cut into 256-row items (two 128-row tiles, A and B); every item streams
+// K[u][:, h] and V[u][:, h] once through shared memory for both tiles, so the
+// context is read once per 256 query rows instead of once per candidate.
+// Work item = (user u, head h, row pair p), p fastest so the items that share
+// a context run side by side and hit L2.  Persistent CTAs take items
+// blockIdx.x, blockIdx.x + gridDim.x, ...
 //
-// Per item and 64-key block j (FlashAttention-style online softmax, base 2,
-// cs = scale * log2(e)):
-//   MMA      S_j = Q . K_j^T            M = 128 rows, N = 64 keys, K = Dh    -> TMEM
-//   softmax  m_j = max(m_{j-1}, rowmax(cs * S_j));  P_j = 2^(cs * S_j - m_j)
-//            (bf16, shared memory);  l = l * 2^(m_{j-1} - m_j) + rowsum(P_j)
-//   MMA      O_j = P_j . V_j            M = 128, N = Dh = 128, K = 64 keys   -> TMEM
-//   softmax  O = O * 2^(m_{j-1} - m_j) + O_j            (fp32 registers)
-// and finally O / l.  The MMA issuer runs S_{j+1} before PV_j, so the
-// softmax of block j + 1 overlaps the PV product of block j.
+// Per tile and 64-key block j (online softmax in base 2, cs = scale*log2(e)):
+//   MMA      S_j = Q . K_j^T          M = 128 rows, N = 64 keys, K = Dh  -> TMEM
+//   softmax  x = cs * S_j;  if max(x) > m + 8 (any lane of the warp): wait
+//            for the PV products so far, rescale O in TMEM and l by 2^(m - m'),
+//            m = m'  (only when the running maximum grows by more than 2^8,
+//            so P = 2^(x - m) <= 256 stays exact enough in bf16);
+//            P_j = 2^(x - m) (bf16, shared memory);  l += rowsum(P_j)
+//   MMA      O += P_j . V_j           M = 128, N = Dh = 128, K = 64 keys -> TMEM
+// and finally O / l.  The issuer runs S two blocks ahead of PV (S_{j+2} of
+// both tiles before PV_j), so the tensor core always has S work queued while
+// the softmax warps produce P.
 //
-// Roles: warp 0 TMA producer (Q once per item; K_j and V_j per block through
-// a 4-stage ring); warp 1 MMA issuer (one thread); warp 2 TMEM allocation;
-// warp 3 lane 1 of CTA 0 validates the offsets; warps 4-7 softmax and output
+// Roles (384 threads): warp 0 TMA producer (Q of both tiles once per item;
+// K_j and V_j per block through separate 3-deep rings, since K_j is consumed
+// two blocks before V_j); warp 1 MMA issuer (one
+// thread); warp 2 TMEM allocation; warp 3 lane 1 of CTA 0 validates the
+// offsets; warps 4-7 softmax and output of tile A, warps 8-11 of tile B
 // (thread = query row = TMEM lane).
 #pragma once
 
@@ -40,21 +45,23 @@
 namespace wst {
 
 constexpr int kAttnDh = 128;          // head dimension (the MMA K of S, N of PV)
-constexpr int kAttnBM = 128;          // query rows per tile
+constexpr int kAttnBM = 128;          // query rows per tile (two tiles per item)
 constexpr int kAttnBN = 64;           // keys per block
-constexpr int kAttnStages = 4;
-constexpr int kAttnThreads = 256;
-constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB: two 64-wide d halves
+constexpr int kAttnStages = 3;        // K ring and V ring depth (each)
+constexpr int kAttnThreads = 384;
+constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB per tile: two 64-wide d halves
 constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 16 KB
-constexpr int kAttnStageBytes = 2 * kAttnKBytes;          // K_j | V_j
 constexpr int kAttnPBytes = kAttnBM * kAttnBN * 2;        // 16 KB
-constexpr int kAttnNumBars = 2 + 2 * kAttnStages + 5 * 2;  // see the kernel's bar map
-constexpr size_t kAttnSmemBytes = (size_t)kAttnQBytes + (size_t)kAttnStages * kAttnStageBytes +
-                                  2 * (size_t)kAttnPBytes + 256 /*barriers*/ + 1024 /*align*/;
+// barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
+// then per tile s_full[2], s_empty[2], p_full[2], pv_done[2], o_empty
+constexpr int kAttnTileBars = 9;
+constexpr int kAttnNumBars = 2 + 4 * kAttnStages + 2 * kAttnTileBars;
+constexpr size_t kAttnSmemBytes = 2 * (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
+                                  4 * (size_t)kAttnPBytes + 512 /*barriers*/ + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
-// TMEM columns: S buffers at 0 and 64, O buffers at 128 and 256.
-constexpr int kAttnTmemS = 0;
-constexpr int kAttnTmemO = 128;
+static_assert(kAttnNumBars * 8 + 8 <= 512, "barrier area");
+// TMEM columns per tile T: S buffers at 256T and 256T + 64, O at 256T + 128.
+constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 
 struct AttnArgs {
   int num_users, num_cand, Lq, H, Lkv;
@@ -83,10 +90,27 @@ __device__ __forceinline__ float attn_ex2(float x) {
   return y;
 }
 
+// Store 32 consecutive fp32 columns of this thread's TMEM lane (warp-wide).
+__device__ __forceinline__ void attn_tmem_store32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]),
+      "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
+      "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void attn_tmem_store_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 struct AttnItem {
   int u, h;
-  int row0;   // first query row of the tile
-  int rows;   // valid query rows (1..128)
+  int row0;        // first query row of tile A (tile B starts 128 rows later)
+  int rows[2];     // valid query rows of tiles A and B (0..128; B may be 0)
 };
 
 // Walks users in order; each role runs its own walker over the same
@@ -94,7 +118,7 @@ struct AttnItem {
 struct AttnWalker {
   int u;
   long long base, count;
-  int q0, nq, tiles;
+  int q0, nq, pairs;
 
   __device__ __forceinline__ void load(const AttnArgs& p) {
     if (u >= p.num_users) { count = 0; return; }
@@ -104,8 +128,8 @@ struct AttnWalker {
     b = min(max(b, a), p.num_cand);
     q0 = a * p.Lq;
     nq = (b - a) * p.Lq;
-    tiles = (nq + kAttnBM - 1) / kAttnBM;
-    count = (long long)tiles * p.H;
+    pairs = (nq + 2 * kAttnBM - 1) / (2 * kAttnBM);
+    count = (long long)pairs * p.H;
   }
   __device__ __forceinline__ void init(const AttnArgs& p) {
     u = 0;
@@ -124,10 +148,12 @@ struct AttnWalker {
     const int r = (int)(t - base);
     AttnItem it;
     it.u = u;
-    it.h = r / tiles;
-    const int qt = r - it.h * tiles;
-    it.row0 = q0 + qt * kAttnBM;
-    it.rows = min(kAttnBM, nq - qt * kAttnBM);
+    it.h = r / pairs;
+    const int pr = r - it.h * pairs;
+    const int left = nq - pr * 2 * kAttnBM;
+    it.row0 = q0 + pr * 2 * kAttnBM;
+    it.rows[0] = min(kAttnBM, left);
+    it.rows[1] = max(0, min(kAttnBM, left - kAttnBM));
     return it;
   }
 };
@@ -150,43 +176,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                    // [2 halves][128 rows][64 d]
-  uint8_t* sKV = sQ + kAttnQBytes;                       // [stage]{K[2][64][64], V[2][64][64]}
-  uint8_t* sP = sKV + kAttnStages * kAttnStageBytes;     // [2][128 rows][64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kAttnPBytes);
+  uint8_t* sQ = smem;                                    // [tile][2 halves][128 rows][64 d]
+  uint8_t* sK = sQ + 2 * kAttnQBytes;                    // [stage][2 halves][64 keys][64 d]
+  uint8_t* sV = sK + kAttnStages * kAttnKBytes;          // [stage][2 halves][64 keys][64 d]
+  uint8_t* sP = sV + kAttnStages * kAttnKBytes;          // [tile][2][128 rows][64 keys]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 4 * kAttnPBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  static_assert(kAttnNumBars * 8 + 8 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t bar_base = smem_addr(bars);
-  // bars: q_full | q_empty | kv_full[S] | kv_empty[S] | s_full[2] | s_empty[2]
-  //       | p_full[2] | pv_done[2] | o_empty[2]  (o_empty follows pv_done)
   const uint32_t q_full = bar_base;
   const uint32_t q_empty = bar_base + 8u;
-  auto kvf_bar = [&](int s) { return bar_base + 8u * (2 + s); };
-  auto kve_bar = [&](int s) { return bar_base + 8u * (2 + kAttnStages + s); };
-  auto sf_bar = [&](int b) { return bar_base + 8u * (2 + 2 * kAttnStages + b); };
-  auto se_bar = [&](int b) { return bar_base + 8u * (4 + 2 * kAttnStages + b); };
-  auto pf_bar = [&](int b) { return bar_base + 8u * (6 + 2 * kAttnStages + b); };
-  auto pv_bar = [&](int b) { return bar_base + 8u * (8 + 2 * kAttnStages + b); };
-  auto oe_bar = [&](int b) { return bar_base + 8u * (10 + 2 * kAttnStages + b); };
-  static_assert(kAttnNumBars == 12 + 2 * kAttnStages, "barrier count");
+  auto kf_bar = [&](int s) { return bar_base + 8u * (2 + s); };
+  auto ke_bar = [&](int s) { return bar_base + 8u * (2 + kAttnStages + s); };
+  auto vf_bar = [&](int s) { return bar_base + 8u * (2 + 2 * kAttnStages + s); };
+  auto ve_bar = [&](int s) { return bar_base + 8u * (2 + 3 * kAttnStages + s); };
+  auto tbar = [&](int T, int k) { return bar_base + 8u * (2 + 4 * kAttnStages + kAttnTileBars * T + k); };
+  auto sf_bar = [&](int T, int b) { return tbar(T, b); };
+  auto se_bar = [&](int T, int b) { return tbar(T, 2 + b); };
+  auto pf_bar = [&](int T, int b) { return tbar(T, 4 + b); };
+  auto pv_bar = [&](int T, int b) { return tbar(T, 6 + b); };
+  auto oe_bar = [&](int T) { return tbar(T, 8); };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(kvf_bar(s), 1);
-      mbar_init(kve_bar(s), 1);
+      mbar_init(kf_bar(s), 1);
+      mbar_init(ke_bar(s), 1);
+      mbar_init(vf_bar(s), 1);
+      mbar_init(ve_bar(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(sf_bar(b), 1);
-      mbar_init(se_bar(b), 4);   // the 4 softmax warps
-      mbar_init(pf_bar(b), 4);
-      mbar_init(pv_bar(b), 1);
-      mbar_init(oe_bar(b), 4);
+    for (int T = 0; T < 2; ++T) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(sf_bar(T, b), 1);
+        mbar_init(se_bar(T, b), 4);   // the tile's 4 softmax warps
+        mbar_init(pf_bar(T, b), 4);
+        mbar_init(pv_bar(T, b), 1);
+      }
+      mbar_init(oe_bar(T), 4);
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -211,29 +241,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       AttnWalker w;
       w.init(p);
-      int stage = 0;
-      uint32_t phase = 0, it = 0;
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0, it = 0;
       bool ok = true;
       for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride, ++it) {
         const AttnItem x = w.item(t);
+        const int ntile = x.rows[1] > 0 ? 2 : 1;
         if (!wait_phase(guard, q_empty, (it & 1u) ^ 1u, (kRoleProducer << 16) | 0x800)) break;
-        mbar_arrive_expect_tx(q_full, kAttnQBytes);
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem_addr(sQ + hf * (kAttnQBytes / 2)), &tmQ, q_full, hf * 64, x.h, x.row0);
+        mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * kAttnQBytes));
+        for (int T = 0; T < ntile; ++T)
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem_addr(sQ + T * kAttnQBytes + hf * (kAttnQBytes / 2)), &tmQ, q_full,
+                        hf * 64, x.h, x.row0 + T * kAttnBM);
         for (int j = 0; j < nblk; ++j) {
-          if (!wait_phase(guard, kve_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
+          if (!wait_phase(guard, ke_bar(ks), kph ^ 1u, (kRoleProducer << 16) | ks)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(kvf_bar(stage), kAttnStageBytes);
-          uint8_t* st = sKV + stage * kAttnStageBytes;
-          for (int hf = 0; hf < 2; ++hf) {
-            attn_tma_load_4d(smem_addr(st + hf * (kAttnKBytes / 2)), &tmK, kvf_bar(stage), hf * 64,
-                             x.h, j * kAttnBN, x.u);
-            attn_tma_load_4d(smem_addr(st + kAttnKBytes + hf * (kAttnKBytes / 2)), &tmV,
-                             kvf_bar(stage), hf * 64, x.h, j * kAttnBN, x.u);
+          mbar_arrive_expect_tx(kf_bar(ks), kAttnKBytes);
+          for (int hf = 0; hf < 2; ++hf)
+            attn_tma_load_4d(smem_addr(sK + ks * kAttnKBytes + hf * (kAttnKBytes / 2)), &tmK, kf_bar(ks),
+                             hf * 64, x.h, j * kAttnBN, x.u);
+          if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
+          if (!wait_phase(guard, ve_bar(vs), vph ^ 1u, (kRoleProducer << 16) | 0x10 | vs)) {
+            ok = false;
+            break;
           }
-          if (++stage == kAttnStages) { stage = 0; phase ^= 1u; }
+          mbar_arrive_expect_tx(vf_bar(vs), kAttnKBytes);
+          for (int hf = 0; hf < 2; ++hf)
+            attn_tma_load_4d(smem_addr(sV + vs * kAttnKBytes + hf * (kAttnKBytes / 2)), &tmV, vf_bar(vs),
+                             hf * 64, x.h, j * kAttnBN, x.u);
+          if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
         }
       }
     }
@@ -241,175 +279,237 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       // S = Q K^T: A = Q (K-major over d), B = K_j (K-major over d).
-      // O = P V:   A = P (K-major over keys), B = V_j (MN-major: d contiguous,
+      // O += P V:  A = P (K-major over keys), B = V_j (MN-major: d contiguous,
       //            two 64-wide d halves 8 KB apart, 16 keys = 2 KB per step).
       constexpr uint32_t idesc_s = idesc_bf16_f32(kAttnBM, kAttnBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kAttnBM, kAttnDh, false, true);
       AttnWalker w;
       w.init(p);
-      int stage = 0;
-      uint32_t phase = 0, it = 0;
-      long long gb = 0;  // blocks issued before this item (buffer parity)
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0, it = 0;
+      long long gb[2] = {0, 0};   // blocks of each tile before this item (buffer parity)
+      uint32_t ni[2] = {0, 0};    // items of each tile before this one (o_empty parity)
       bool ok = true;
       for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride, ++it) {
+        const AttnItem x = w.item(t);
+        const int ntile = x.rows[1] > 0 ? 2 : 1;
         if (!wait_phase(guard, q_full, it & 1u, (kRoleMma << 16) | 0x800)) break;
         tc_fence_after_sync();
-        int prev_stage = 0;
-        for (int j = 0; j <= nblk && ok; ++j) {
-          const int cur_stage = stage;
+        // Step j: S_j of both tiles (if j < nblk), then PV_{j-2} (if j >= 2).
+        for (int j = 0; j < nblk + 2 && ok; ++j) {
           if (j < nblk) {
-            const long long g = gb + j;
-            const int b = (int)(g & 1);
-            const uint32_t ph = (uint32_t)((g >> 1) & 1);
-            if (!wait_phase(guard, kvf_bar(stage), phase, (kRoleMma << 16) | stage) ||
-                !wait_phase(guard, se_bar(b), ph ^ 1u, (kRoleMma << 16) | 0x100 | b)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t qB = smem_addr(sQ);
-            const uint32_t kB = smem_addr(sKV + stage * kAttnStageBytes);
-            const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + b * kAttnBN);
+            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
+            const uint64_t kd0 = sdesc_sw128(smem_addr(sK + ks * kAttnKBytes), 16, 1024);
+            for (int T = 0; T < ntile; ++T) {
+              const long long g = gb[T] + j;
+              const int b = (int)(g & 1);
+              if (!wait_phase(guard, se_bar(T, b), (uint32_t)((g >> 1) & 1) ^ 1u,
+                              (kRoleMma << 16) | 0x100 | (T << 4) | b)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              const uint64_t qd0 = sdesc_sw128(smem_addr(sQ + T * kAttnQBytes), 16, 1024);
+              const uint32_t d_s = tmem_base + (uint32_t)(256 * T + kAttnBN * b);
 #pragma unroll
-            for (int kk = 0; kk < kAttnDh / 16; ++kk) {
-              const uint32_t off = (uint32_t)((kk & 3) * 32);  // 16 d = 32 B
-              const uint64_t ad = sdesc_sw128(qB + (kk >> 2) * (kAttnQBytes / 2) + off, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kB + (kk >> 2) * (kAttnKBytes / 2) + off, 16, 1024);
-              umma_bf16<1>(d_s, ad, bd, idesc_s, kk != 0 ? 1u : 0u);
+              for (int kk = 0; kk < kAttnDh / 16; ++kk) {
+                // 16 d = 32 B within a 64-wide half; halves 16 KB (Q) / 8 KB (K) apart
+                const uint32_t qo = (uint32_t)((kk >> 2) * (kAttnQBytes / 2) + (kk & 3) * 32);
+                const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
+                umma_bf16<1>(d_s, qd0 + (qo >> 4), kd0 + (ko >> 4), idesc_s, kk != 0 ? 1u : 0u);
+              }
+              umma_commit(sf_bar(T, b));
             }
-            umma_commit(sf_bar(b));
+            if (!ok) break;
+            umma_commit(ke_bar(ks));
             if (j == nblk - 1) umma_commit(q_empty);
-            if (++stage == kAttnStages) { stage = 0; phase ^= 1u; }
+            if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
           }
-          if (j >= 1) {
-            const long long g = gb + j - 1;
-            const int b = (int)(g & 1);
-            const uint32_t ph = (uint32_t)((g >> 1) & 1);
-            if (!wait_phase(guard, pf_bar(b), ph, (kRoleMma << 16) | 0x200 | b) ||
-                !wait_phase(guard, oe_bar(b), ph ^ 1u, (kRoleMma << 16) | 0x300 | b)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t pB = smem_addr(sP + b * kAttnPBytes);
-            const uint32_t vB = smem_addr(sKV + prev_stage * kAttnStageBytes + kAttnKBytes);
-            const uint32_t d_o = tmem_base + (uint32_t)(kAttnTmemO + b * kAttnDh);
+          if (j >= 2) {
+            const int jj = j - 2;
+            if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs)) { ok = false; break; }
+            const uint64_t vd0 = sdesc_sw128(smem_addr(sV + vs * kAttnKBytes), kAttnKBytes / 2, 1024);
+            for (int T = 0; T < ntile; ++T) {
+              const long long g = gb[T] + jj;
+              const int b = (int)(g & 1);
+              if (!wait_phase(guard, pf_bar(T, b), (uint32_t)((g >> 1) & 1),
+                              (kRoleMma << 16) | 0x200 | (T << 4) | b) ||
+                  (jj == 0 && !wait_phase(guard, oe_bar(T), (ni[T] & 1u) ^ 1u,
+                                          (kRoleMma << 16) | 0x300 | (T << 4)))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              const uint64_t pd0 = sdesc_sw128(smem_addr(sP + (2 * T + b) * kAttnPBytes), 16, 1024);
+              const uint32_t d_o = tmem_base + (uint32_t)(256 * T + 128);
 #pragma unroll
-            for (int kk = 0; kk < kAttnBN / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(pB + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(vB + kk * 2048, kAttnKBytes / 2, 1024);
-              umma_bf16<1>(d_o, ad, bd, idesc_o, kk != 0 ? 1u : 0u);
+              for (int kk = 0; kk < kAttnBN / 16; ++kk)  // 16 keys: 32 B of P, 2 KB of V
+                umma_bf16<1>(d_o, pd0 + (uint32_t)(kk * 2), vd0 + (uint32_t)(kk * 128), idesc_o,
+                             (jj > 0 || kk != 0) ? 1u : 0u);
+              umma_commit(pv_bar(T, b));
             }
-            umma_commit(pv_bar(b));
-            umma_commit(kve_bar(prev_stage));
+            if (!ok) break;
+            umma_commit(ve_bar(vs));
+            if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
           }
-          prev_stage = cur_stage;
         }
-        gb += nblk;
+        for (int T = 0; T < ntile; ++T) {
+          gb[T] += nblk;
+          ++ni[T];
+        }
       }
     }
   } else if (warp == 3) {
     if (lane == 1 && blockIdx.x == 0) attn_check_offsets(p);
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + output
+    const int T = (warp - 4) >> 2;        // tile A (warps 4-7) or B (warps 8-11)
     const int q = warp & 3;
     const int row = q * 32 + (int)lane;  // query row of the tile = TMEM lane
-    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16);
+    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(256 * T);
+    const uint32_t t_o = t_lane + 128;
     AttnWalker w;
     w.init(p);
     long long gb = 0;
     bool ok = true;
     for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride) {
       const AttnItem x = w.item(t);
-      float o[kAttnDh];
+      if (x.rows[T] == 0) continue;  // tile B of a short item: idle
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j < nblk; ++j) {
+        const long long g = gb + j;
+        const int b = (int)(g & 1);
+        const uint32_t ph = (uint32_t)((g >> 1) & 1);
+        if (!warp_wait_phase(guard, sf_bar(T, b), ph, (kRoleEpilogue << 16) | (T << 4) | b)) { ok = false; break; }
+        tc_fence_after_sync();
+        float s[kAttnBN];
+        tmem_load32(t_lane + kAttnBN * b, *reinterpret_cast<float(*)[32]>(s));
+        tmem_load32(t_lane + kAttnBN * b + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(se_bar(T, b));
+        // Row extremum of the raw scores (the maximum of cs * s is cs * max s
+        // for cs >= 0 and cs * min s otherwise); keys past the end of the
+        // context (last block only) take no part and get no weight.
+        const int kvalid = p.Lkv - j * kAttnBN;
+        const float cs = p.scale_log2;
+        const bool pos = cs >= 0.0f;
+        float e8[8];
 #pragma unroll
-      for (int i = 0; i < kAttnDh; ++i) o[i] = 0.0f;
-      float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
-      for (int j = 0; j <= nblk; ++j) {
-        float alpha = 0.0f;
-        if (j < nblk) {
-          const long long g = gb + j;
-          const int b = (int)(g & 1);
-          const uint32_t ph = (uint32_t)((g >> 1) & 1);
-          if (!warp_wait_phase(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
-          tc_fence_after_sync();
-          float s[kAttnBN];
-          tmem_load32(t_lane + kAttnTmemS + b * kAttnBN, *reinterpret_cast<float(*)[32]>(s));
-          tmem_load32(t_lane + kAttnTmemS + b * kAttnBN + 32, *reinterpret_cast<float(*)[32]>(s + 32));
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(se_bar(b));
-          // Keys past the end of the context (last block only) take no weight.
-          const int kvalid = p.Lkv - j * kAttnBN;
-          float mx = -INFINITY;
+        for (int i = 0; i < 8; ++i) e8[i] = pos ? -INFINITY : INFINITY;
+        if (kvalid >= kAttnBN) {
+#pragma unroll
+          for (int i = 0; i < kAttnBN; ++i) e8[i & 7] = pos ? fmaxf(e8[i & 7], s[i]) : fminf(e8[i & 7], s[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kAttnBN; ++i)
+            if (i < kvalid) e8[i & 7] = pos ? fmaxf(e8[i & 7], s[i]) : fminf(e8[i & 7], s[i]);
+        }
+        float ext;
+        if (pos)
+          ext = fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])), fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])));
+        else
+          ext = fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
+        const float mx = ext * cs;
+        if (j == 0) {
+          m = mx;  // the first PV product overwrites O: nothing to rescale
+        } else {
+          const bool grow = mx > m + kAttnRescaleLog2;
+          if (__any_sync(0xffffffffu, grow)) {
+            // O holds the PV products of blocks < j: wait for the last one,
+            // then rescale O and l of the rows whose maximum grew.
+            const long long gp = g - 1;
+            if (!warp_wait_phase(guard, pv_bar(T, (int)(gp & 1)), (uint32_t)((gp >> 1) & 1),
+                                 (kRoleEpilogue << 16) | 0x100 | (T << 4))) { ok = false; break; }
+            tc_fence_after_sync();
+            const float alpha = grow ? attn_ex2(m - mx) : 1.0f;
+            if (grow) {
+              l *= alpha;
+              m = mx;
+            }
+#pragma unroll
+            for (int c = 0; c < kAttnDh / 32; ++c) {
+              float v[32];
+              tmem_load32(t_o + c * 32, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= alpha;
+              attn_tmem_store32(t_o + c * 32, v);
+            }
+            attn_tmem_store_wait();
+            tc_fence_before_sync();
+          }
+        }
+        // P = 2^(cs * s - m), one FFMA and one ex2 per score.
+        float rs8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rs8[i] = 0.0f;
+        if (kvalid >= kAttnBN) {
 #pragma unroll
           for (int i = 0; i < kAttnBN; ++i) {
-            s[i] = i < kvalid ? s[i] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, s[i]);
+            s[i] = attn_ex2(fmaf(s[i], cs, -m));
+            rs8[i & 7] += s[i];
           }
-          const float m_new = fmaxf(m, mx);
-          alpha = attn_ex2(m - m_new);
-          float rs = 0.0f;
+        } else {
 #pragma unroll
           for (int i = 0; i < kAttnBN; ++i) {
-            s[i] = attn_ex2(s[i] - m_new);
-            rs += s[i];
+            s[i] = i < kvalid ? attn_ex2(fmaf(s[i], cs, -m)) : 0.0f;
+            rs8[i & 7] += s[i];
           }
-          l = l * alpha + rs;
-          m = m_new;
-          // P_j row -> shared memory, 128-byte swizzled K-major layout:
-          // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
-          const uint32_t prow = smem_addr(sP + b * kAttnPBytes) + (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
-#pragma unroll
-          for (int c = 0; c < kAttnBN / 8; ++c) {
-            st_shared_v4(prow + (uint32_t)(((c ^ (row & 7)) & 7) * 16),
-                         pack_bf16x2(s[8 * c + 0], s[8 * c + 1]), pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
-                         pack_bf16x2(s[8 * c + 4], s[8 * c + 5]), pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(pf_bar(b));
         }
-        if (j >= 1) {
-          // O = O * alpha_{j-1} + P_{j-1} V_{j-1}
-          const long long g = gb + j - 1;
-          const int b = (int)(g & 1);
-          const uint32_t ph = (uint32_t)((g >> 1) & 1);
-          if (!warp_wait_phase(guard, pv_bar(b), ph, (kRoleEpilogue << 16) | 0x100 | b)) { ok = false; break; }
-          tc_fence_after_sync();
-#pragma unroll
-          for (int c = 0; c < kAttnDh / 32; ++c) {
-            float v[32];
-            tmem_load32(t_lane + kAttnTmemO + b * kAttnDh + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha_prev, v[i]);
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(oe_bar(b));
+        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        // The P buffer was last read by the PV product of block g - 2.
+        if (!warp_wait_phase(guard, pv_bar(T, b), ph ^ 1u, (kRoleEpilogue << 16) | 0x200 | (T << 4) | b)) {
+          ok = false;
+          break;
         }
-        alpha_prev = alpha;
+        // P_j row -> shared memory, 128-byte swizzled K-major layout:
+        // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
+        const uint32_t prow = smem_addr(sP + (2 * T + b) * kAttnPBytes) +
+                              (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+#pragma unroll
+        for (int c = 0; c < kAttnBN / 8; ++c) {
+          st_shared_v4(prow + (uint32_t)(((c ^ (row & 7)) & 7) * 16),
+                       pack_bf16x2(s[8 * c + 0], s[8 * c + 1]), pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
+                       pack_bf16x2(s[8 * c + 4], s[8 * c + 5]), pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pf_bar(T, b));
       }
       if (!ok) break;
+      // Output: wait for the last PV product, read O, divide by l, store.
+      const long long gl = gb + nblk - 1;
+      if (!warp_wait_phase(guard, pv_bar(T, (int)(gl & 1)), (uint32_t)((gl >> 1) & 1),
+                           (kRoleEpilogue << 16) | 0x300 | (T << 4))) { ok = false; break; }
+      tc_fence_after_sync();
       gb += nblk;
-      if (row < x.rows) {
-        const float inv = 1.0f / l;
-        const long long base = ((long long)(x.row0 + row) * p.H + x.h) * kAttnDh;
-        if constexpr (OUT_F32) {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + base);
+      const float inv = 1.0f / l;
+      const bool store = row < x.rows[T];
+      const long long base = ((long long)(x.row0 + T * kAttnBM + row) * p.H + x.h) * kAttnDh;
 #pragma unroll
-          for (int i = 0; i < kAttnDh / 4; ++i)
-            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + base);
+      for (int c = 0; c < kAttnDh / 32; ++c) {
+        float v[32];
+        tmem_load32(t_o + c * 32, v);
+        if (store) {
+          if constexpr (OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + base + c * 32);
 #pragma unroll
-          for (int i = 0; i < kAttnDh / 8; ++i)
-            dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
-                                pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                                pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                                pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + base + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                  pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                  pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                  pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+          }
         }
       }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(oe_bar(T));
     }
   }
 
