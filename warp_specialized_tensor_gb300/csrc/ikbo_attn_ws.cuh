@@ -26,14 +26,20 @@
 //            for the PV products so far, rescale O in TMEM and l by 2^(m - m'),
 //            m = m'  (only when the running maximum grows by more than 2^8,
 //            so P = 2^(x - m) <= 256 stays exact enough in bf16);
-//            P_j = 2^(x - m) (bf16, shared memory);  l += rowsum(P_j)
-//   MMA      O += P_j . V_j           M = 128, N = Dh = 128, K = 64 keys -> TMEM
-// and finally O / l.  The issuer runs S two blocks ahead of PV (S_{j+2} of
-// both tiles before PV_j), so the tensor core always has S work queued while
-// the softmax warps produce P.
+//            P_j = 2^(x - m) as bf16 pairs written back over S_j's TMEM
+//            columns;  l += rowsum(P_j)
+//   MMA      O += P_j . V_j           A = P_j from TMEM, B = V_j from shared
+//                                     memory; M = 128, N = Dh, K = 64 keys
+// and finally O / l.  P never touches shared memory: with these small MMAs
+// the operand reads from shared memory, not the tensor math, set the pace
+// (measured on GB300: a P round trip through shared memory cost a quarter
+// of the kernel's time).  Each tile has two S/P buffers; the issuer queues
+// PV_{j-2} and then S_j, which overwrites the buffer PV_{j-2} reads (the
+// tensor core runs one thread's MMAs in issue order), so S runs two blocks
+// ahead of PV and the tensor core has S work queued while P is produced.
 //
 // Roles (384 threads): warp 0 TMA producer (Q of both tiles once per item;
-// K_j and V_j per block through separate 3-deep rings, since K_j is consumed
+// K_j and V_j per block through separate 4-deep rings, since K_j is consumed
 // two blocks before V_j); warp 1 MMA issuer (one
 // thread); warp 2 TMEM allocation; warp 3 lane 1 of CTA 0 validates the
 // offsets; warps 4-7 softmax and output of tile A, warps 8-11 of tile B
@@ -47,20 +53,20 @@ namespace wst {
 constexpr int kAttnDh = 128;          // head dimension (the MMA K of S, N of PV)
 constexpr int kAttnBM = 128;          // query rows per tile (two tiles per item)
 constexpr int kAttnBN = 64;           // keys per block
-constexpr int kAttnStages = 3;        // K ring and V ring depth (each)
+constexpr int kAttnStages = 4;        // K ring and V ring depth (each)
 constexpr int kAttnThreads = 384;
 constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB per tile: two 64-wide d halves
 constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 16 KB
-constexpr int kAttnPBytes = kAttnBM * kAttnBN * 2;        // 16 KB
 // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
-// then per tile s_full[2], s_empty[2], p_full[2], pv_done[2], o_empty
-constexpr int kAttnTileBars = 9;
+// then per tile s_full[2], p_full[2], pv_done[2], o_empty
+constexpr int kAttnTileBars = 7;
 constexpr int kAttnNumBars = 2 + 4 * kAttnStages + 2 * kAttnTileBars;
 constexpr size_t kAttnSmemBytes = 2 * (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
-                                  4 * (size_t)kAttnPBytes + 512 /*barriers*/ + 1024 /*align*/;
+                                  512 /*barriers*/ + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kAttnNumBars * 8 + 8 <= 512, "barrier area");
-// TMEM columns per tile T: S buffers at 256T and 256T + 64, O at 256T + 128.
+// TMEM columns per tile T: S/P buffers at 256T and 256T + 64 (P as bf16
+// pairs in the first 32 columns of its S buffer), O at 256T + 128.
 constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 
 struct AttnArgs {
@@ -105,6 +111,18 @@ __device__ __forceinline__ void attn_tmem_store32(uint32_t taddr, const float (&
 
 __device__ __forceinline__ void attn_tmem_store_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// tcgen05.mma (cta_group::1, kind::f16) with the A operand in TMEM: lane r
+// holds row r, each 32-bit column two consecutive K elements (low half first).
+__device__ __forceinline__ void attn_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 struct AttnItem {
@@ -179,8 +197,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sQ = smem;                                    // [tile][2 halves][128 rows][64 d]
   uint8_t* sK = sQ + 2 * kAttnQBytes;                    // [stage][2 halves][64 keys][64 d]
   uint8_t* sV = sK + kAttnStages * kAttnKBytes;          // [stage][2 halves][64 keys][64 d]
-  uint8_t* sP = sV + kAttnStages * kAttnKBytes;          // [tile][2][128 rows][64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 4 * kAttnPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnStages * kAttnKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -195,10 +212,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto ve_bar = [&](int s) { return bar_base + 8u * (2 + 3 * kAttnStages + s); };
   auto tbar = [&](int T, int k) { return bar_base + 8u * (2 + 4 * kAttnStages + kAttnTileBars * T + k); };
   auto sf_bar = [&](int T, int b) { return tbar(T, b); };
-  auto se_bar = [&](int T, int b) { return tbar(T, 2 + b); };
-  auto pf_bar = [&](int T, int b) { return tbar(T, 4 + b); };
-  auto pv_bar = [&](int T, int b) { return tbar(T, 6 + b); };
-  auto oe_bar = [&](int T) { return tbar(T, 8); };
+  auto pf_bar = [&](int T, int b) { return tbar(T, 2 + b); };
+  auto pv_bar = [&](int T, int b) { return tbar(T, 4 + b); };
+  auto oe_bar = [&](int T) { return tbar(T, 6); };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -212,8 +228,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int T = 0; T < 2; ++T) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(sf_bar(T, b), 1);
-        mbar_init(se_bar(T, b), 4);   // the tile's 4 softmax warps
-        mbar_init(pf_bar(T, b), 4);
+        mbar_init(pf_bar(T, b), 4);   // the tile's 4 softmax warps
         mbar_init(pv_bar(T, b), 1);
       }
       mbar_init(oe_bar(T), 4);
@@ -295,36 +310,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int ntile = x.rows[1] > 0 ? 2 : 1;
         if (!wait_phase(guard, q_full, it & 1u, (kRoleMma << 16) | 0x800)) break;
         tc_fence_after_sync();
-        // Step j: S_j of both tiles (if j < nblk), then PV_{j-2} (if j >= 2).
+        // Step j: PV_{j-2} of both tiles (if j >= 2), then S_j (if j < nblk).
+        // S_j overwrites the TMEM buffer that holds P_{j-2}; the tensor core
+        // performs this thread's MMAs in issue order, so PV_{j-2} reads P
+        // before S_j writes there.  (PV_{j-2} waited for the softmax to
+        // finish block j-2, so S_{j-2} has been read as well.)
         for (int j = 0; j < nblk + 2 && ok; ++j) {
-          if (j < nblk) {
-            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
-            const uint64_t kd0 = sdesc_sw128(smem_addr(sK + ks * kAttnKBytes), 16, 1024);
-            for (int T = 0; T < ntile; ++T) {
-              const long long g = gb[T] + j;
-              const int b = (int)(g & 1);
-              if (!wait_phase(guard, se_bar(T, b), (uint32_t)((g >> 1) & 1) ^ 1u,
-                              (kRoleMma << 16) | 0x100 | (T << 4) | b)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after_sync();
-              const uint64_t qd0 = sdesc_sw128(smem_addr(sQ + T * kAttnQBytes), 16, 1024);
-              const uint32_t d_s = tmem_base + (uint32_t)(256 * T + kAttnBN * b);
-#pragma unroll
-              for (int kk = 0; kk < kAttnDh / 16; ++kk) {
-                // 16 d = 32 B within a 64-wide half; halves 16 KB (Q) / 8 KB (K) apart
-                const uint32_t qo = (uint32_t)((kk >> 2) * (kAttnQBytes / 2) + (kk & 3) * 32);
-                const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
-                umma_bf16<1>(d_s, qd0 + (qo >> 4), kd0 + (ko >> 4), idesc_s, kk != 0 ? 1u : 0u);
-              }
-              umma_commit(sf_bar(T, b));
-            }
-            if (!ok) break;
-            umma_commit(ke_bar(ks));
-            if (j == nblk - 1) umma_commit(q_empty);
-            if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
-          }
           if (j >= 2) {
             const int jj = j - 2;
             if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs)) { ok = false; break; }
@@ -340,17 +331,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
               }
               tc_fence_after_sync();
-              const uint64_t pd0 = sdesc_sw128(smem_addr(sP + (2 * T + b) * kAttnPBytes), 16, 1024);
+              const uint32_t a_p = tmem_base + (uint32_t)(256 * T + kAttnBN * b);
               const uint32_t d_o = tmem_base + (uint32_t)(256 * T + 128);
 #pragma unroll
-              for (int kk = 0; kk < kAttnBN / 16; ++kk)  // 16 keys: 32 B of P, 2 KB of V
-                umma_bf16<1>(d_o, pd0 + (uint32_t)(kk * 2), vd0 + (uint32_t)(kk * 128), idesc_o,
-                             (jj > 0 || kk != 0) ? 1u : 0u);
+              for (int kk = 0; kk < kAttnBN / 16; ++kk)  // 16 keys: 8 TMEM columns of P, 2 KB of V
+                attn_mma_ts(d_o, a_p + (uint32_t)(kk * 8), vd0 + (uint32_t)(kk * 128), idesc_o,
+                            (jj > 0 || kk != 0) ? 1u : 0u);
               umma_commit(pv_bar(T, b));
             }
             if (!ok) break;
             umma_commit(ve_bar(vs));
             if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
+          }
+          if (j < nblk) {
+            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint64_t kd0 = sdesc_sw128(smem_addr(sK + ks * kAttnKBytes), 16, 1024);
+            for (int T = 0; T < ntile; ++T) {
+              const int b = (int)((gb[T] + j) & 1);
+              const uint64_t qd0 = sdesc_sw128(smem_addr(sQ + T * kAttnQBytes), 16, 1024);
+              const uint32_t d_s = tmem_base + (uint32_t)(256 * T + kAttnBN * b);
+#pragma unroll
+              for (int kk = 0; kk < kAttnDh / 16; ++kk) {
+                // 16 d = 32 B within a 64-wide half; halves 16 KB (Q) / 8 KB (K) apart
+                const uint32_t qo = (uint32_t)((kk >> 2) * (kAttnQBytes / 2) + (kk & 3) * 32);
+                const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
+                umma_bf16<1>(d_s, qd0 + (qo >> 4), kd0 + (ko >> 4), idesc_s, kk != 0 ? 1u : 0u);
+              }
+              umma_commit(sf_bar(T, b));
+            }
+            umma_commit(ke_bar(ks));
+            if (j == nblk - 1) umma_commit(q_empty);
+            if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
           }
         }
         for (int T = 0; T < ntile; ++T) {
@@ -385,9 +397,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float s[kAttnBN];
         tmem_load32(t_lane + kAttnBN * b, *reinterpret_cast<float(*)[32]>(s));
         tmem_load32(t_lane + kAttnBN * b + 32, *reinterpret_cast<float(*)[32]>(s + 32));
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(se_bar(T, b));
         // Row extremum of the raw scores (the maximum of cs * s is cs * max s
         // for cs >= 0 and cs * min s otherwise); keys past the end of the
         // context (last block only) take no part and get no weight.
@@ -457,22 +466,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        // The P buffer was last read by the PV product of block g - 2.
-        if (!warp_wait_phase(guard, pv_bar(T, b), ph ^ 1u, (kRoleEpilogue << 16) | 0x200 | (T << 4) | b)) {
-          ok = false;
-          break;
-        }
-        // P_j row -> shared memory, 128-byte swizzled K-major layout:
-        // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
-        const uint32_t prow = smem_addr(sP + (2 * T + b) * kAttnPBytes) +
-                              (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+        // P_j -> TMEM as bf16 pairs over the first 32 columns of S_j's buffer
+        // (the A operand of the PV product), then hand it to the MMA issuer.
+        {
+          float pk[32];
 #pragma unroll
-        for (int c = 0; c < kAttnBN / 8; ++c) {
-          st_shared_v4(prow + (uint32_t)(((c ^ (row & 7)) & 7) * 16),
-                       pack_bf16x2(s[8 * c + 0], s[8 * c + 1]), pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
-                       pack_bf16x2(s[8 * c + 4], s[8 * c + 5]), pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
+          for (int c = 0; c < 32; ++c) pk[c] = __uint_as_float(pack_bf16x2(s[2 * c], s[2 * c + 1]));
+          attn_tmem_store32(t_lane + kAttnBN * b, pk);
         }
-        fence_proxy_async_smem();
+        attn_tmem_store_wait();
+        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(pf_bar(T, b));
       }
