@@ -54,7 +54,7 @@ int launch_attn(const AttnProblem& pr, const DeviceInfo& dev, cudaStream_t strea
   // Persistent grid: one CTA per SM, no more than the items can use (the
   // per-user item counts live on the device: bound them by H * (items + users)).
   const long long items_max =
-      (long long)pr.H * ((long long)((nq + 2 * kAttnBM - 1) / (2 * kAttnBM)) + pr.num_users);
+      (long long)pr.H * ((long long)((nq + kAttnBM - 1) / kAttnBM) + pr.num_users);
   const long long grid = std::max(1LL, std::min<long long>(dev.num_sms, items_max));
   if ((st = ensure_smem_attr((const void*)kern, kAttnSmemBytes))) return st;
   cudaLaunchConfig_t cfg{};

@@ -13,15 +13,15 @@
 //     O[r][h] = sum_j softmax_j(scale * Q[r][h] . K[u][j][h]) * V[u][j][h]
 //
 // In-kernel broadcast: the query rows of ALL candidates of user u are stacked
-// and cut into 256-row items (two 128-row tiles, A and B); every item streams
-// K[u][:, h] and V[u][:, h] once through shared memory for both tiles, so the
-// context is read once per 256 query rows instead of once per candidate.
-// Work item = (user u, head h, row pair p), p fastest so the items that share
-// a context run side by side and hit L2.  Persistent CTAs take items
-// blockIdx.x, blockIdx.x + gridDim.x, ...
+// and cut into 128-row tiles; every tile streams K[u][:, h] and V[u][:, h]
+// once, so the context is read once per 128 query rows instead of once per
+// candidate.  Work item = (user u, head h, query tile t), with t fastest so
+// the tiles that share a context run side by side and hit L2.  Persistent
+// CTAs take items blockIdx.x, blockIdx.x + gridDim.x, ...
 //
-// Per tile and 64-key block j (online softmax in base 2, cs = scale*log2(e)):
-//   MMA      S_j = Q . K_j^T          M = 128 rows, N = 64 keys, K = Dh  -> TMEM
+// Per item and 128-key block j (online softmax in base 2, cs = scale*log2(e)):
+//   MMA      S_j = Q . K_j^T          A = Q from TMEM, B = K_j from shared
+//                                     memory; M = 128 rows, N = 128 keys, K = Dh
 //   softmax  x = cs * S_j;  if max(x) > m + 8 (any lane of the warp): wait
 //            for the PV products so far, rescale O in TMEM and l by 2^(m - m'),
 //            m = m'  (only when the running maximum grows by more than 2^8,
@@ -29,21 +29,24 @@
 //            P_j = 2^(x - m) as bf16 pairs written back over S_j's TMEM
 //            columns;  l += rowsum(P_j)
 //   MMA      O += P_j . V_j           A = P_j from TMEM, B = V_j from shared
-//                                     memory; M = 128, N = Dh, K = 64 keys
-// and finally O / l.  P never touches shared memory: with these small MMAs
-// the operand reads from shared memory, not the tensor math, set the pace
-// (measured on GB300: a P round trip through shared memory cost a quarter
-// of the kernel's time).  Each tile has two S/P buffers; the issuer queues
-// PV_{j-2} and then S_j, which overwrites the buffer PV_{j-2} reads (the
-// tensor core runs one thread's MMAs in issue order), so S runs two blocks
-// ahead of PV and the tensor core has S work queued while P is produced.
+//                                     memory; M = 128, N = Dh, K = 128 keys
+// and finally O / l.  Q and P live in TMEM: with MMAs this small, operand
+// reads from shared memory rather than the tensor math set the pace
+// (measured on GB300: Q and P read from shared memory cost about half of
+// the kernel's time), so shared memory only feeds K and V.  TMEM holds Q
+// (64 columns of bf16 pairs), two S/P buffers of 128 columns and O (128).
+// (128-key blocks: with 64 keys the N = 64 products ran at about half the
+// tensor rate and the per-block handshakes doubled.)
+// The issuer queues PV_{j-2} and then S_j, which overwrites the buffer
+// PV_{j-2} reads (the tensor core runs one thread's MMAs in issue order), so
+// S runs two blocks ahead of PV and the softmax always finds S ready.
 //
-// Roles (384 threads): warp 0 TMA producer (Q of both tiles once per item;
-// K_j and V_j per block through separate 4-deep rings, since K_j is consumed
-// two blocks before V_j); warp 1 MMA issuer (one
-// thread); warp 2 TMEM allocation; warp 3 lane 1 of CTA 0 validates the
-// offsets; warps 4-7 softmax and output of tile A, warps 8-11 of tile B
-// (thread = query row = TMEM lane).
+// Roles (256 threads): warp 0 TMA producer (Q once per item into a staging
+// buffer; K_j and V_j per block through separate 3-deep rings, since K_j is
+// consumed two blocks before V_j); warp 1 MMA issuer (one thread); warp 2
+// TMEM allocation; warp 3 lane 1 of CTA 0 validates the offsets; warps 4-7
+// copy Q into TMEM, run the softmax and write the output (thread = query
+// row = TMEM lane).
 #pragma once
 
 #include "wst_common.cuh"
@@ -51,22 +54,25 @@
 namespace wst {
 
 constexpr int kAttnDh = 128;          // head dimension (the MMA K of S, N of PV)
-constexpr int kAttnBM = 128;          // query rows per tile (two tiles per item)
-constexpr int kAttnBN = 64;           // keys per block
-constexpr int kAttnStages = 4;        // K ring and V ring depth (each)
-constexpr int kAttnThreads = 384;
-constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB per tile: two 64-wide d halves
-constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 16 KB
-// barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
-// then per tile s_full[2], p_full[2], pv_done[2], o_empty
-constexpr int kAttnTileBars = 7;
-constexpr int kAttnNumBars = 2 + 4 * kAttnStages + 2 * kAttnTileBars;
-constexpr size_t kAttnSmemBytes = 2 * (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
+constexpr int kAttnBM = 128;          // query rows per tile
+constexpr int kAttnBN = 128;          // keys per block
+constexpr int kAttnStages = 3;        // K ring and V ring depth (each)
+constexpr int kAttnThreads = 256;
+constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB: two 64-wide d halves
+constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 32 KB: two 64-wide d halves
+// barriers: q_full, q_empty, qt_full, k_full[S], k_empty[S], v_full[S],
+// v_empty[S], s_full[2], p_full[2], pv_done[2], o_empty
+constexpr int kAttnNumBars = 3 + 4 * kAttnStages + 7;
+constexpr size_t kAttnSmemBytes = (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
                                   512 /*barriers*/ + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kAttnNumBars * 8 + 8 <= 512, "barrier area");
-// TMEM columns per tile T: S/P buffers at 256T and 256T + 64 (P as bf16
-// pairs in the first 32 columns of its S buffer), O at 256T + 128.
+// TMEM columns: Q at 0 (64 columns of bf16 pairs), S/P buffers at 64 and
+// 192 (P as bf16 pairs in the first 64 columns of its S buffer), O at 320.
+constexpr int kAttnTmemQ = 0;
+constexpr int kAttnTmemS = 64;
+constexpr int kAttnTmemO = 320;
+static_assert(kAttnTmemO + kAttnDh <= 512, "TMEM columns");
 constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 
 struct AttnArgs {
@@ -127,8 +133,8 @@ __device__ __forceinline__ void attn_mma_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 struct AttnItem {
   int u, h;
-  int row0;        // first query row of tile A (tile B starts 128 rows later)
-  int rows[2];     // valid query rows of tiles A and B (0..128; B may be 0)
+  int row0;   // first query row of the tile
+  int rows;   // valid query rows (1..128)
 };
 
 // Walks users in order; each role runs its own walker over the same
@@ -136,7 +142,7 @@ struct AttnItem {
 struct AttnWalker {
   int u;
   long long base, count;
-  int q0, nq, pairs;
+  int q0, nq, tiles;
 
   __device__ __forceinline__ void load(const AttnArgs& p) {
     if (u >= p.num_users) { count = 0; return; }
@@ -146,8 +152,8 @@ struct AttnWalker {
     b = min(max(b, a), p.num_cand);
     q0 = a * p.Lq;
     nq = (b - a) * p.Lq;
-    pairs = (nq + 2 * kAttnBM - 1) / (2 * kAttnBM);
-    count = (long long)pairs * p.H;
+    tiles = (nq + kAttnBM - 1) / kAttnBM;
+    count = (long long)tiles * p.H;
   }
   __device__ __forceinline__ void init(const AttnArgs& p) {
     u = 0;
@@ -166,12 +172,10 @@ struct AttnWalker {
     const int r = (int)(t - base);
     AttnItem it;
     it.u = u;
-    it.h = r / pairs;
-    const int pr = r - it.h * pairs;
-    const int left = nq - pr * 2 * kAttnBM;
-    it.row0 = q0 + pr * 2 * kAttnBM;
-    it.rows[0] = min(kAttnBM, left);
-    it.rows[1] = max(0, min(kAttnBM, left - kAttnBM));
+    it.h = r / tiles;
+    const int qt = r - it.h * tiles;
+    it.row0 = q0 + qt * kAttnBM;
+    it.rows = min(kAttnBM, nq - qt * kAttnBM);
     return it;
   }
 };
@@ -194,8 +198,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                    // [tile][2 halves][128 rows][64 d]
-  uint8_t* sK = sQ + 2 * kAttnQBytes;                    // [stage][2 halves][64 keys][64 d]
+  uint8_t* sQ = smem;                                    // [2 halves][128 rows][64 d] staging
+  uint8_t* sK = sQ + kAttnQBytes;                        // [stage][2 halves][64 keys][64 d]
   uint8_t* sV = sK + kAttnStages * kAttnKBytes;          // [stage][2 halves][64 keys][64 d]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnStages * kAttnKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
@@ -204,35 +208,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t bar_base = smem_addr(bars);
-  const uint32_t q_full = bar_base;
-  const uint32_t q_empty = bar_base + 8u;
-  auto kf_bar = [&](int s) { return bar_base + 8u * (2 + s); };
-  auto ke_bar = [&](int s) { return bar_base + 8u * (2 + kAttnStages + s); };
-  auto vf_bar = [&](int s) { return bar_base + 8u * (2 + 2 * kAttnStages + s); };
-  auto ve_bar = [&](int s) { return bar_base + 8u * (2 + 3 * kAttnStages + s); };
-  auto tbar = [&](int T, int k) { return bar_base + 8u * (2 + 4 * kAttnStages + kAttnTileBars * T + k); };
-  auto sf_bar = [&](int T, int b) { return tbar(T, b); };
-  auto pf_bar = [&](int T, int b) { return tbar(T, 2 + b); };
-  auto pv_bar = [&](int T, int b) { return tbar(T, 4 + b); };
-  auto oe_bar = [&](int T) { return tbar(T, 6); };
+  const uint32_t q_full = bar_base;          // Q tile landed in the staging buffer
+  const uint32_t q_empty = bar_base + 8u;    // staging buffer copied into TMEM
+  const uint32_t qt_full = bar_base + 16u;   // Q in TMEM (4 softmax warps)
+  auto kf_bar = [&](int s) { return bar_base + 8u * (3 + s); };
+  auto ke_bar = [&](int s) { return bar_base + 8u * (3 + kAttnStages + s); };
+  auto vf_bar = [&](int s) { return bar_base + 8u * (3 + 2 * kAttnStages + s); };
+  auto ve_bar = [&](int s) { return bar_base + 8u * (3 + 3 * kAttnStages + s); };
+  auto sf_bar = [&](int b) { return bar_base + 8u * (3 + 4 * kAttnStages + b); };
+  auto pf_bar = [&](int b) { return bar_base + 8u * (5 + 4 * kAttnStages + b); };
+  auto pv_bar = [&](int b) { return bar_base + 8u * (7 + 4 * kAttnStages + b); };
+  const uint32_t oe_bar = bar_base + 8u * (9 + 4 * kAttnStages);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, 4);
+    mbar_init(qt_full, 4);
     for (int s = 0; s < kAttnStages; ++s) {
       mbar_init(kf_bar(s), 1);
       mbar_init(ke_bar(s), 1);
       mbar_init(vf_bar(s), 1);
       mbar_init(ve_bar(s), 1);
     }
-    for (int T = 0; T < 2; ++T) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(sf_bar(T, b), 1);
-        mbar_init(pf_bar(T, b), 4);   // the tile's 4 softmax warps
-        mbar_init(pv_bar(T, b), 1);
-      }
-      mbar_init(oe_bar(T), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sf_bar(b), 1);
+      mbar_init(pf_bar(b), 4);   // the 4 softmax warps
+      mbar_init(pv_bar(b), 1);
     }
+    mbar_init(oe_bar, 4);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -261,13 +264,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = true;
       for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride, ++it) {
         const AttnItem x = w.item(t);
-        const int ntile = x.rows[1] > 0 ? 2 : 1;
         if (!wait_phase(guard, q_empty, (it & 1u) ^ 1u, (kRoleProducer << 16) | 0x800)) break;
-        mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * kAttnQBytes));
-        for (int T = 0; T < ntile; ++T)
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(smem_addr(sQ + T * kAttnQBytes + hf * (kAttnQBytes / 2)), &tmQ, q_full,
-                        hf * 64, x.h, x.row0 + T * kAttnBM);
+        mbar_arrive_expect_tx(q_full, kAttnQBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(smem_addr(sQ + hf * (kAttnQBytes / 2)), &tmQ, q_full, hf * 64, x.h, x.row0);
         for (int j = 0; j < nblk; ++j) {
           if (!wait_phase(guard, ke_bar(ks), kph ^ 1u, (kRoleProducer << 16) | ks)) {
             ok = false;
@@ -293,110 +293,127 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // S = Q K^T: A = Q (K-major over d), B = K_j (K-major over d).
-      // O += P V:  A = P (K-major over keys), B = V_j (MN-major: d contiguous,
-      //            two 64-wide d halves 8 KB apart, 16 keys = 2 KB per step).
+      // S = Q K^T: A = Q (TMEM), B = K_j (K-major over d: two 64-wide halves
+      //            8 KB apart, 16 d = 32 B per step).
+      // O += P V:  A = P (TMEM), B = V_j (MN-major: d contiguous, two 64-wide
+      //            d halves 8 KB apart, 16 keys = 2 KB per step).
       constexpr uint32_t idesc_s = idesc_bf16_f32(kAttnBM, kAttnBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kAttnBM, kAttnDh, false, true);
+      const uint32_t a_q = tmem_base + kAttnTmemQ;
+      const uint32_t d_o = tmem_base + kAttnTmemO;
       AttnWalker w;
       w.init(p);
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0, it = 0;
-      long long gb[2] = {0, 0};   // blocks of each tile before this item (buffer parity)
-      uint32_t ni[2] = {0, 0};    // items of each tile before this one (o_empty parity)
+      long long gb = 0;  // blocks before this item (buffer parity)
       bool ok = true;
       for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride, ++it) {
-        const AttnItem x = w.item(t);
-        const int ntile = x.rows[1] > 0 ? 2 : 1;
-        if (!wait_phase(guard, q_full, it & 1u, (kRoleMma << 16) | 0x800)) break;
+        if (!wait_phase(guard, qt_full, it & 1u, (kRoleMma << 16) | 0x800)) break;
         tc_fence_after_sync();
-        // Step j: PV_{j-2} of both tiles (if j >= 2), then S_j (if j < nblk).
-        // S_j overwrites the TMEM buffer that holds P_{j-2}; the tensor core
+        // Step j: PV_{j-2} (if j >= 2), then S_j (if j < nblk).  S_j
+        // overwrites the TMEM buffer that holds P_{j-2}; the tensor core
         // performs this thread's MMAs in issue order, so PV_{j-2} reads P
-        // before S_j writes there.  (PV_{j-2} waited for the softmax to
-        // finish block j-2, so S_{j-2} has been read as well.)
+        // before S_j writes there (and PV_{j-2} waited for the softmax to
+        // finish block j-2, so S_{j-2} has been read as well).
         for (int j = 0; j < nblk + 2 && ok; ++j) {
           if (j >= 2) {
             const int jj = j - 2;
-            if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs)) { ok = false; break; }
-            const uint64_t vd0 = sdesc_sw128(smem_addr(sV + vs * kAttnKBytes), kAttnKBytes / 2, 1024);
-            for (int T = 0; T < ntile; ++T) {
-              const long long g = gb[T] + jj;
-              const int b = (int)(g & 1);
-              if (!wait_phase(guard, pf_bar(T, b), (uint32_t)((g >> 1) & 1),
-                              (kRoleMma << 16) | 0x200 | (T << 4) | b) ||
-                  (jj == 0 && !wait_phase(guard, oe_bar(T), (ni[T] & 1u) ^ 1u,
-                                          (kRoleMma << 16) | 0x300 | (T << 4)))) {
-                ok = false;
-                break;
-              }
-              tc_fence_after_sync();
-              const uint32_t a_p = tmem_base + (uint32_t)(256 * T + kAttnBN * b);
-              const uint32_t d_o = tmem_base + (uint32_t)(256 * T + 128);
-#pragma unroll
-              for (int kk = 0; kk < kAttnBN / 16; ++kk)  // 16 keys: 8 TMEM columns of P, 2 KB of V
-                attn_mma_ts(d_o, a_p + (uint32_t)(kk * 8), vd0 + (uint32_t)(kk * 128), idesc_o,
-                            (jj > 0 || kk != 0) ? 1u : 0u);
-              umma_commit(pv_bar(T, b));
+            const long long g = gb + jj;
+            const int b = (int)(g & 1);
+            if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
+                !wait_phase(guard, pf_bar(b), (uint32_t)((g >> 1) & 1), (kRoleMma << 16) | 0x200 | b) ||
+                (jj == 0 && !wait_phase(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
+              ok = false;
+              break;
             }
-            if (!ok) break;
+            tc_fence_after_sync();
+            const uint64_t vd0 = sdesc_sw128(smem_addr(sV + vs * kAttnKBytes), kAttnKBytes / 2, 1024);
+            const uint32_t a_p = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
+#pragma unroll
+            for (int kk = 0; kk < kAttnBN / 16; ++kk)  // 16 keys: 8 TMEM columns of P, 2 KB of V
+              attn_mma_ts(d_o, a_p + (uint32_t)(kk * 8), vd0 + (uint32_t)(kk * 128), idesc_o,
+                          (jj > 0 || kk != 0) ? 1u : 0u);
+            umma_commit(pv_bar(b));
             umma_commit(ve_bar(vs));
             if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
           }
           if (j < nblk) {
             if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
             tc_fence_after_sync();
+            const int b = (int)((gb + j) & 1);
             const uint64_t kd0 = sdesc_sw128(smem_addr(sK + ks * kAttnKBytes), 16, 1024);
-            for (int T = 0; T < ntile; ++T) {
-              const int b = (int)((gb[T] + j) & 1);
-              const uint64_t qd0 = sdesc_sw128(smem_addr(sQ + T * kAttnQBytes), 16, 1024);
-              const uint32_t d_s = tmem_base + (uint32_t)(256 * T + kAttnBN * b);
+            const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
 #pragma unroll
-              for (int kk = 0; kk < kAttnDh / 16; ++kk) {
-                // 16 d = 32 B within a 64-wide half; halves 16 KB (Q) / 8 KB (K) apart
-                const uint32_t qo = (uint32_t)((kk >> 2) * (kAttnQBytes / 2) + (kk & 3) * 32);
-                const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
-                umma_bf16<1>(d_s, qd0 + (qo >> 4), kd0 + (ko >> 4), idesc_s, kk != 0 ? 1u : 0u);
-              }
-              umma_commit(sf_bar(T, b));
+            for (int kk = 0; kk < kAttnDh / 16; ++kk) {
+              // 16 d: 8 TMEM columns of Q; 32 B within a 64-wide half of K (16 KB apart)
+              const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
+              attn_mma_ts(d_s, a_q + (uint32_t)(kk * 8), kd0 + (ko >> 4), idesc_s, kk != 0 ? 1u : 0u);
             }
+            umma_commit(sf_bar(b));
             umma_commit(ke_bar(ks));
-            if (j == nblk - 1) umma_commit(q_empty);
             if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
           }
         }
-        for (int T = 0; T < ntile; ++T) {
-          gb[T] += nblk;
-          ++ni[T];
-        }
+        gb += nblk;
       }
     }
   } else if (warp == 3) {
     if (lane == 1 && blockIdx.x == 0) attn_check_offsets(p);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------------ softmax + output
-    const int T = (warp - 4) >> 2;        // tile A (warps 4-7) or B (warps 8-11)
+    // ------------------------------------------------------------------ Q copy, softmax, output
     const int q = warp & 3;
     const int row = q * 32 + (int)lane;  // query row of the tile = TMEM lane
-    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(256 * T);
-    const uint32_t t_o = t_lane + 128;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16);
+    const uint32_t t_o = t_lane + kAttnTmemO;
+    // Q row of item `it` -> TMEM (64 columns of bf16 pairs), then release
+    // the staging buffer and tell the MMA issuer.
+    auto copy_q = [&](uint32_t it) -> bool {
+      if (!warp_wait_phase(guard, q_full, it & 1u, (kRoleEpilogue << 16) | 0x400)) return false;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float qv[32];
+        const uint32_t qrow = smem_addr(sQ + hf * (kAttnQBytes / 2)) + (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
+          uint32_t a, b2, c2, d;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a), "=r"(b2), "=r"(c2), "=r"(d)
+                       : "r"(qrow + (uint32_t)(((c ^ (row & 7)) & 7) * 16)));
+          qv[4 * c + 0] = __uint_as_float(a);
+          qv[4 * c + 1] = __uint_as_float(b2);
+          qv[4 * c + 2] = __uint_as_float(c2);
+          qv[4 * c + 3] = __uint_as_float(d);
+        }
+        attn_tmem_store32(t_lane + kAttnTmemQ + hf * 32, qv);
+      }
+      attn_tmem_store_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(q_empty);
+        mbar_arrive(qt_full);
+      }
+      return true;
+    };
     AttnWalker w;
     w.init(p);
     long long gb = 0;
-    bool ok = true;
-    for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride) {
+    uint32_t it = 0;
+    long long t = blockIdx.x;
+    bool ok = w.seek(p, t) && copy_q(0);
+    while (ok) {
       const AttnItem x = w.item(t);
-      if (x.rows[T] == 0) continue;  // tile B of a short item: idle
       float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nblk; ++j) {
         const long long g = gb + j;
         const int b = (int)(g & 1);
         const uint32_t ph = (uint32_t)((g >> 1) & 1);
-        if (!warp_wait_phase(guard, sf_bar(T, b), ph, (kRoleEpilogue << 16) | (T << 4) | b)) { ok = false; break; }
+        if (!warp_wait_phase(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
         tc_fence_after_sync();
         float s[kAttnBN];
-        tmem_load32(t_lane + kAttnBN * b, *reinterpret_cast<float(*)[32]>(s));
-        tmem_load32(t_lane + kAttnBN * b + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+#pragma unroll
+        for (int c = 0; c < kAttnBN / 32; ++c)
+          tmem_load32(t_lane + kAttnTmemS + kAttnBN * b + 32 * c, *reinterpret_cast<float(*)[32]>(s + 32 * c));
         // Row extremum of the raw scores (the maximum of cs * s is cs * max s
         // for cs >= 0 and cs * min s otherwise); keys past the end of the
         // context (last block only) take no part and get no weight.
@@ -428,8 +445,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // O holds the PV products of blocks < j: wait for the last one,
             // then rescale O and l of the rows whose maximum grew.
             const long long gp = g - 1;
-            if (!warp_wait_phase(guard, pv_bar(T, (int)(gp & 1)), (uint32_t)((gp >> 1) & 1),
-                                 (kRoleEpilogue << 16) | 0x100 | (T << 4))) { ok = false; break; }
+            if (!warp_wait_phase(guard, pv_bar((int)(gp & 1)), (uint32_t)((gp >> 1) & 1),
+                                 (kRoleEpilogue << 16) | 0x100)) { ok = false; break; }
             tc_fence_after_sync();
             const float alpha = grow ? attn_ex2(m - mx) : 1.0f;
             if (grow) {
@@ -445,7 +462,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               attn_tmem_store32(t_o + c * 32, v);
             }
             attn_tmem_store_wait();
-            tc_fence_before_sync();
           }
         }
         // P = 2^(cs * s - m), one FFMA and one ex2 per score.
@@ -466,29 +482,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        // P_j -> TMEM as bf16 pairs over the first 32 columns of S_j's buffer
+        // P_j -> TMEM as bf16 pairs over the first 64 columns of S_j's buffer
         // (the A operand of the PV product), then hand it to the MMA issuer.
-        {
+#pragma unroll
+        for (int h2 = 0; h2 < kAttnBN / 64; ++h2) {
           float pk[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = __uint_as_float(pack_bf16x2(s[2 * c], s[2 * c + 1]));
-          attn_tmem_store32(t_lane + kAttnBN * b, pk);
+          for (int c = 0; c < 32; ++c)
+            pk[c] = __uint_as_float(pack_bf16x2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1]));
+          attn_tmem_store32(t_lane + kAttnTmemS + kAttnBN * b + 32 * h2, pk);
         }
         attn_tmem_store_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pf_bar(T, b));
+        if (lane == 0) mbar_arrive(pf_bar(b));
       }
       if (!ok) break;
+      // Bring the next item's Q into TMEM before this item's output, so its
+      // first S products overlap the epilogue.  Every S product of this item
+      // (the readers of Q in TMEM) completed before the last s_full above.
+      t += stride;
+      ++it;
+      const bool more = w.seek(p, t);
+      if (more && !copy_q(it)) break;
       // Output: wait for the last PV product, read O, divide by l, store.
       const long long gl = gb + nblk - 1;
-      if (!warp_wait_phase(guard, pv_bar(T, (int)(gl & 1)), (uint32_t)((gl >> 1) & 1),
-                           (kRoleEpilogue << 16) | 0x300 | (T << 4))) { ok = false; break; }
+      if (!warp_wait_phase(guard, pv_bar((int)(gl & 1)), (uint32_t)((gl >> 1) & 1),
+                           (kRoleEpilogue << 16) | 0x300)) { ok = false; break; }
       tc_fence_after_sync();
       gb += nblk;
       const float inv = 1.0f / l;
-      const bool store = row < x.rows[T];
-      const long long base = ((long long)(x.row0 + T * kAttnBM + row) * p.H + x.h) * kAttnDh;
+      const bool store = row < x.rows;
+      const long long base = ((long long)(x.row0 + row) * p.H + x.h) * kAttnDh;
 #pragma unroll
       for (int c = 0; c < kAttnDh / 32; ++c) {
         float v[32];
@@ -512,7 +537,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(oe_bar(T));
+      if (lane == 0) mbar_arrive(oe_bar);
+      if (!more) break;
     }
   }
 
