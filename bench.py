@@ -15,6 +15,10 @@ than L2 (129 MB), so L2 is not flushed between steps.
 
 --impl reference times the CPU oracle (fp64, all host cores) on a bounded
 sample of the same workload, as the reference arm.
+
+Besides the step, the JSON line carries `parity_workloads`: dense 256^3, the
+skinny batched GEMM, the RMSNorm-fused GEMM and IKBO attention, each timed on
+its own (`--only rmsnorm|attention` times one of the last two alone).
 """
 from __future__ import annotations
 
@@ -221,7 +225,11 @@ def run_ours(args, rank, world, dist):
     wst.load_library()
     peaks = load_peaks()
 
-    need = (args.only,) if args.only else ("dense", "grouped", "ikbo")
+    extra_only = {"rmsnorm": "dense8192_rmsnorm", "attention": "ikbo_attention"}.get(args.only)
+    if extra_only:
+        need = ()
+    else:
+        need = (args.only,) if args.only else ("dense", "grouped", "ikbo")
     host = {}
     d = g = k = None
     if "dense" in need:
@@ -254,6 +262,11 @@ def run_ours(args, rank, world, dist):
     kernels = [("dense", k_dense), ("grouped", k_grouped), ("ikbo", k_ikbo)]
     if args.only:
         kernels = [kv for kv in kernels if kv[0] == args.only]
+    if extra_only:
+        out = time_parity_workloads(wst, torch, dev, stream, peaks, ws, names=(extra_only,),
+                                    iters=max(1, args.steps))
+        return {"metric": "extra workload timing (profiling run; not a bench line)",
+                "only": extra_only, "parity_workloads": out}
     flops = {"dense": dense_flops(**DENSE), "grouped": grouped_flops(**GROUPED),
              "ikbo": ikbo_flops(**IKBO)}
     nbytes = {"dense": dense_bytes(**DENSE), "grouped": grouped_bytes(**GROUPED),
@@ -360,7 +373,7 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize(dev)
         ctx["torch_matmul_dense_tflops"] = round(flops["dense"] * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e12, 1)
 
-    # ---- the two parity-only workloads, timed on their own (not in the step)
+    # ---- the extra workloads (parity cases and next rows), timed on their own
     extra = {}
     if not args.only and not args.no_extra:
         extra = time_parity_workloads(wst, torch, dev, stream, peaks, ws)
@@ -385,7 +398,10 @@ def run_ours(args, rank, world, dist):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(ach / peaks["bf16_tflops"], 4),
                 "traffic": committed_traffic(dom),
-                "peak_source": peaks["source"] + " (burst bf16, cuBLAS)"}
+                "peak_source": peaks["source"] + " (burst bf16, cuBLAS)",
+                # context: the same kernel against the power-capped sustained figure
+                "peak_sustained": peaks["bf16_tflops_sustained"],
+                "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4)}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -409,48 +425,58 @@ def run_ours(args, rank, world, dist):
     return result
 
 
-def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20):
+def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20, names=None):
     """dense 256^3 (fp32 out; launch-latency bound), the skinny recsys batch
     (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2), the
     row-RMSNorm-fused GEMM on the dense 8192^3 operands, and IKBO attention."""
     import synthetic
     out = {}
-    cases = []
-    d1 = synthetic.workload("dense256")
-    A1, B1 = d1["A"].to(dev), d1["B"].to(dev)
-    C1 = torch.empty(256, 256, dtype=torch.float32, device=dev)
-    cases.append(("dense256", lambda: wst.wst_gemm_bf16(A1, B1, C1, workspace=ws, stream=stream),
-                  dense_flops(256, 256, 256), dense_bytes(256, 256, 256, out_bytes=4)))
-    d5 = synthetic.workload("skinny_batch")
-    A5, B5, b5 = d5["A"].to(dev), d5["B"].to(dev), d5["bias"].to(dev)
-    C5 = torch.empty(512, 1024, 256, dtype=torch.bfloat16, device=dev)
-    cases.append(("skinny_batch",
-                  lambda: wst.wst_gemm_bf16(A5, B5, C5, bias=b5, epi="bias_silu", workspace=ws,
-                                            stream=stream),
-                  dense_flops(1024, 256, 512, batch=512),
-                  dense_bytes(1024, 256, 512, batch=512) + 512 * 256 * 2))
-    # the fused row-RMSNorm GEMM on the dense 8192^3 operands (single-CTA tiles)
-    d2 = synthetic.workload("dense8192")
-    A2, B2 = d2["A"].to(dev), d2["B"].to(dev)
-    C2 = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev)
-    cases.append(("dense8192_rmsnorm",
-                  lambda: wst.wst_gemm_rmsnorm_bf16(A2, B2, C2, eps=1e-6, workspace=ws, stream=stream),
-                  dense_flops(8192, 8192, 8192), dense_bytes(8192, 8192, 8192)))
-    # IKBO attention: 32 users x 256 candidates x 2 query rows, 4 heads, Dh 128,
-    # 2048 context rows per user; bf16 out.  FLOPs: QK^T and PV; bytes: Q, the
-    # users' K and V once, O.
-    d6 = synthetic.workload("ikbo_attention")
-    Q6, K6, V6 = d6["Q"].to(dev), d6["K"].to(dev), d6["V"].to(dev)
-    off6 = d6["user_offsets"].to(dev)
-    O6 = torch.empty(Q6.shape, dtype=torch.bfloat16, device=dev)
-    nq6, H6, Dh6 = Q6.shape
-    Lkv6 = K6.shape[1]
-    cases.append(("ikbo_attention",
-                  lambda: wst.wst_ikbo_attention_bf16(Q6, K6, V6, off6, O6, Lq=d6["Lq"],
-                                                      workspace=ws, stream=stream),
-                  4.0 * nq6 * Lkv6 * Dh6 * H6,
-                  2 * (2 * nq6 * H6 * Dh6) + 2 * (2 * K6.numel())))
-    for name, fn, fl, by in cases:
+
+    def dense256():
+        d1 = synthetic.workload("dense256")
+        A1, B1 = d1["A"].to(dev), d1["B"].to(dev)
+        C1 = torch.empty(256, 256, dtype=torch.float32, device=dev)
+        return (lambda: wst.wst_gemm_bf16(A1, B1, C1, workspace=ws, stream=stream),
+                dense_flops(256, 256, 256), dense_bytes(256, 256, 256, out_bytes=4))
+
+    def skinny_batch():
+        d5 = synthetic.workload("skinny_batch")
+        A5, B5, b5 = d5["A"].to(dev), d5["B"].to(dev), d5["bias"].to(dev)
+        C5 = torch.empty(512, 1024, 256, dtype=torch.bfloat16, device=dev)
+        return (lambda: wst.wst_gemm_bf16(A5, B5, C5, bias=b5, epi="bias_silu", workspace=ws,
+                                          stream=stream),
+                dense_flops(1024, 256, 512, batch=512),
+                dense_bytes(1024, 256, 512, batch=512) + 512 * 256 * 2)
+
+    def dense8192_rmsnorm():
+        # the fused row-RMSNorm GEMM on the dense 8192^3 operands
+        d2 = synthetic.workload("dense8192")
+        A2, B2 = d2["A"].to(dev), d2["B"].to(dev)
+        C2 = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev)
+        return (lambda: wst.wst_gemm_rmsnorm_bf16(A2, B2, C2, eps=1e-6, workspace=ws, stream=stream),
+                dense_flops(8192, 8192, 8192), dense_bytes(8192, 8192, 8192))
+
+    def ikbo_attention():
+        # 32 users x 256 candidates x 2 query rows, 4 heads, Dh 128, 2048
+        # context rows per user; bf16 out.  FLOPs: QK^T and PV; bytes: Q, the
+        # users' K and V once, O.
+        d6 = synthetic.workload("ikbo_attention")
+        Q6, K6, V6 = d6["Q"].to(dev), d6["K"].to(dev), d6["V"].to(dev)
+        off6 = d6["user_offsets"].to(dev)
+        O6 = torch.empty(Q6.shape, dtype=torch.bfloat16, device=dev)
+        nq6, H6, Dh6 = Q6.shape
+        Lkv6 = K6.shape[1]
+        return (lambda: wst.wst_ikbo_attention_bf16(Q6, K6, V6, off6, O6, Lq=d6["Lq"],
+                                                    workspace=ws, stream=stream),
+                4.0 * nq6 * Lkv6 * Dh6 * H6,
+                2 * (2 * nq6 * H6 * Dh6) + 2 * (2 * K6.numel()))
+
+    builders = [("dense256", dense256), ("skinny_batch", skinny_batch),
+                ("dense8192_rmsnorm", dense8192_rmsnorm), ("ikbo_attention", ikbo_attention)]
+    for name, build in builders:
+        if names is not None and name not in names:
+            continue
+        fn, fl, by = build()
         for _ in range(3):
             fn()
         torch.cuda.synchronize(dev)
@@ -596,9 +622,10 @@ def main():
     ap.add_argument("--no-context", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip timing the two parity-only workloads")
-    ap.add_argument("--only", choices=["dense", "grouped", "ikbo"], default=None,
-                    help="time one kernel only (profiling runs); not a bench line")
+                    help="skip timing the extra workloads (parity cases and next rows)")
+    ap.add_argument("--only", choices=["dense", "grouped", "ikbo", "rmsnorm", "attention"], default=None,
+                    help="time one kernel only (profiling runs); not a bench line. rmsnorm and "
+                         "attention time that extra workload alone")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KEY", "REGEX"),

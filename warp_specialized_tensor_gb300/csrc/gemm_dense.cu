@@ -169,7 +169,9 @@ int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   int st = current_device_info(&dev);
   if (st) return st;
   if (pr.grouped) return run_gemm_grouped(pr, dev, stream);
-  if (pr.norm) return dispatch<1, true>(pr, dev, stream);  // row statistics: single-CTA tiles
+  if (pr.norm)
+    return dense_cta_group(pr.M) == 2 ? dispatch<2, true>(pr, dev, stream)
+                                      : dispatch<1, true>(pr, dev, stream);
   return dense_cta_group(pr.M) == 2 ? dispatch<2, false>(pr, dev, stream)
                                     : dispatch<1, false>(pr, dev, stream);
 }

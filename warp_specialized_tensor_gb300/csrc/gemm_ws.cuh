@@ -143,7 +143,6 @@ struct GemmCfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kWarpCols % kColsPerChunk == 0, "epilogue chunking");
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
-  static_assert(!NORM || CG == 1, "row normalisation runs on single-CTA tiles");
 };
 
 // NORM: C = epi(r[m] * (A.B^T)[m][n] (+ bias)), r[m] = 1/sqrt(mean_k A[m][k]^2
@@ -151,7 +150,11 @@ struct GemmCfg {
 // lane one row: eight 16-byte swizzled chunks per stage), accumulate the
 // row's sum of squares in fp32, release the stage together with the MMA, and
 // hand 1/sqrt(ss/K + eps) per row to the epilogue through a double-buffered
-// shared array.  The norm costs no extra pass over A in HBM.
+// shared array.  The norm costs no extra pass over A in HBM.  In a CTA pair
+// both CTAs' loads complete on the leader's full[s], which the peer's stats
+// warps cannot wait on: the leader's MMA thread, once full[s] completes,
+// arrives on landed[s] in both CTAs, and the stats warps wait on their own
+// landed[s].
 //
 // CG = 2: a cluster of two CTAs computes one 256 x BN tile with
 // tcgen05.mma.cta_group::2 issued by the even CTA (the leader).  Each CTA
@@ -173,7 +176,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
   float* row_scale = reinterpret_cast<float*>(smStg + EPI_WARPS * Cfg::kStageBufs * Cfg::kStgBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(row_scale) + Cfg::kScaleBytes);
   // bars: full[STAGES] | empty[STAGES] | acc_full[2] | acc_empty[2] | scale_full[2] | scale_empty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 8);
+  //       | landed[STAGES]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 8);
+  static_assert((3 * STAGES + 8) * 8 + 8 <= 256, "barrier area");
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -185,6 +190,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
   auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
   auto sclf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 4 + a); };
   auto scle_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 6 + a); };
+  auto land_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + 8 + s); };
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;   // CTA rank in the pair
   const long long cluster_id = blockIdx.x / CG;
   const long long num_clusters = gridDim.x / CG;
@@ -193,6 +199,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1 + Cfg::kStatsWarps);  // MMA commit (+ stats warps)
+      mbar_init(land_bar(s), 1);                       // the leader's MMA thread (NORM pairs)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
@@ -292,6 +299,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             ok = false;
             break;
           }
+          if constexpr (NORM && CG == 2) {
+            // both CTAs' A stages have landed: release the stats warps
+            mbar_arrive(land_bar(stage));
+            mbar_arrive_cluster(map_to_cta(land_bar(stage), 1));
+          }
           tc_fence_after_sync();
           const uint32_t aBase = smem_addr(smA + stage * Cfg::kABytes);
           const uint32_t bBase = smem_addr(smB + stage * Cfg::kBBytes);
@@ -324,11 +336,18 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
       float ss = 0.0f;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        if (!warp_wait_phase(guard, full_bar(stage), phase, (kRoleEpilogue << 16) | 0x400 | stage)) {
+        // this CTA's A stage has landed (full[s] of a single CTA; landed[s],
+        // signalled by the leader's MMA thread, in a pair)
+        const uint32_t ready = CG == 2 ? land_bar(stage) : full_bar(stage);
+        const bool got = CG == 2
+            ? warp_wait_phase_cluster(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage)
+            : warp_wait_phase(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage);
+        if (!got) {
           ok = false;
           break;
         }
-        (void)mbar_try_wait(full_bar(stage), phase);  // each lane acquires the completed phase
+        if constexpr (CG == 2) (void)mbar_try_wait_cluster(ready, phase);  // each lane acquires the phase
+        else (void)mbar_try_wait(ready, phase);
         const uint32_t row_addr = smem_addr(smA + stage * Cfg::kABytes) + (uint32_t)r * 128u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
