@@ -150,11 +150,14 @@ struct GemmCfg {
 // lane one row: eight 16-byte swizzled chunks per stage), accumulate the
 // row's sum of squares in fp32, release the stage together with the MMA, and
 // hand 1/sqrt(ss/K + eps) per row to the epilogue through a double-buffered
-// shared array.  The norm costs no extra pass over A in HBM.  In a CTA pair
-// both CTAs' loads complete on the leader's full[s], which the peer's stats
-// warps cannot wait on: the leader's MMA thread, once full[s] completes,
-// arrives on landed[s] in both CTAs, and the stats warps wait on their own
-// landed[s].
+// shared array.  The norm costs no extra pass over A in HBM.  The stats
+// warps read a stage after the MMAs that use it: the MMA issuer's per-stage
+// commit goes to consumed[s] (in both CTAs of a pair, by the commit's
+// multicast) instead of empty[s], and the stats warps release empty[s] once
+// they have read the stage.  (In a pair, both CTAs' loads complete on the
+// leader's full[s], which the peer's warps cannot wait on; relaying full[s]
+// to the peer with a thread's remote arrive per stage ran 2.6x slower on
+// GB300.)
 //
 // CG = 2: a cluster of two CTAs computes one 256 x BN tile with
 // tcgen05.mma.cta_group::2 issued by the even CTA (the leader).  Each CTA
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
   float* row_scale = reinterpret_cast<float*>(smStg + EPI_WARPS * Cfg::kStageBufs * Cfg::kStgBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(row_scale) + Cfg::kScaleBytes);
   // bars: full[STAGES] | empty[STAGES] | acc_full[2] | acc_empty[2] | scale_full[2] | scale_empty[2]
-  //       | landed[STAGES]
+  //       | consumed[STAGES] (NORM)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 8);
   static_assert((3 * STAGES + 8) * 8 + 8 <= 256, "barrier area");
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
   auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
   auto sclf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 4 + a); };
   auto scle_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 6 + a); };
-  auto land_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + 8 + s); };
+  auto cons_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + 8 + s); };
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;   // CTA rank in the pair
   const long long cluster_id = blockIdx.x / CG;
   const long long num_clusters = gridDim.x / CG;
@@ -198,8 +201,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1 + Cfg::kStatsWarps);  // MMA commit (+ stats warps)
-      mbar_init(land_bar(s), 1);                       // the leader's MMA thread (NORM pairs)
+      // released by the MMA commit, or (NORM) by the stats warps, which wait
+      // for the MMA commit on consumed[s]
+      mbar_init(empty_bar(s), NORM ? Cfg::kStatsWarps : 1);
+      mbar_init(cons_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
@@ -299,11 +304,6 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             ok = false;
             break;
           }
-          if constexpr (NORM && CG == 2) {
-            // both CTAs' A stages have landed: release the stats warps
-            mbar_arrive(land_bar(stage));
-            mbar_arrive_cluster(map_to_cta(land_bar(stage), 1));
-          }
           tc_fence_after_sync();
           const uint32_t aBase = smem_addr(smA + stage * Cfg::kABytes);
           const uint32_t bBase = smem_addr(smB + stage * Cfg::kBBytes);
@@ -313,9 +313,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             const uint64_t bd = sdesc_sw128(bBase + k * 32, 16, 1024);
             umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          // slot free (in both CTAs) once these MMAs finish
-          if constexpr (CG == 1) umma_commit(empty_bar(stage));
-          else                   umma_commit_pair(empty_bar(stage), 0x3);
+          // slot free (in both CTAs) once these MMAs finish; with the row
+          // statistics, once the stats warps have read it after them
+          const uint32_t rel = NORM ? cons_bar(stage) : empty_bar(stage);
+          if constexpr (CG == 1) umma_commit(rel);
+          else                   umma_commit_pair(rel, 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -336,9 +338,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
       float ss = 0.0f;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        // this CTA's A stage has landed (full[s] of a single CTA; landed[s],
-        // signalled by the leader's MMA thread, in a pair)
-        const uint32_t ready = CG == 2 ? land_bar(stage) : full_bar(stage);
+        // the MMAs that read this stage completed (their commit, multicast
+        // to both CTAs of a pair, arrives on consumed[s])
+        const uint32_t ready = cons_bar(stage);
         const bool got = CG == 2
             ? warp_wait_phase_cluster(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage)
             : warp_wait_phase(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage);
