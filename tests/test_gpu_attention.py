@@ -105,3 +105,30 @@ def test_attention_bad_offsets_latched(wst):
     d["user_offsets"] = torch.tensor([0, 20, 5, 30], dtype=torch.int32)
     O, st = run(wst, d)
     assert st == wst.WST_ERR_BAD_OFFSETS
+
+
+def test_attention_rescale_path(wst):
+    # Keys of later blocks scaled up so that row maxima grow by far more than
+    # 2^8 between blocks: the kernel must rescale O in tensor memory (the
+    # N(0,1) cases above never take that branch).
+    d = synthetic.ikbo_attention(users=2, cand_per_user=[70, 9], Lq=2, H=2, Lkv=400, seed=8)
+    K = d["K"].float()
+    K[:, 128:256] *= 6.0
+    K[:, 256:] *= 14.0
+    d["K"] = K.to(torch.bfloat16)
+    for out in (torch.float32, torch.bfloat16):
+        O, st = run(wst, d, out)
+        assert st == 0
+        ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 2)
+        check(O, ref, d["V"], out == torch.bfloat16, what="rescale")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_attention_negative_and_zero_scale(wst, scale):
+    # scale < 0: the row extremum is the minimum of the raw scores; scale = 0:
+    # uniform weights over the context (the mean of V).
+    d = synthetic.ikbo_attention(users=3, cand_per_user=[20, 0, 45], Lq=1, H=2, Lkv=300, seed=9)
+    O, st = run(wst, d, torch.float32, scale=scale)
+    assert st == 0
+    ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 1, scale=scale)
+    check(O, ref, d["V"], False, what="scale %g" % scale)
