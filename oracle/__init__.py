@@ -99,7 +99,7 @@ def num_threads() -> int:
     return _load().oracle_num_threads()
 
 
-EPI = {"none": 0, "bias": 1, "bias_silu": 2}
+EPI = {"none": 0, "bias": 1, "bias_silu": 2, "bias_gelu": 3}
 
 
 def gemm(A, B, bias=None, epi: str = "none", rows=None) -> np.ndarray:

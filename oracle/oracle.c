@@ -19,8 +19,10 @@
  *                blocked loop computes C[m][n] = sum_k A[m][k] * B[k][n].
  *                Written here as that definition, one k at a time.
  *   epilogue  -- [P1] "Five key areas" (model-aware fusion) names fusing
- *                elementwise work into the matmul; the bias + SiLU form is
- *                bias added first, then SiLU(x) = x / (1 + exp(-x)).
+ *                elementwise work into the matmul; the bias + activation
+ *                forms add the bias first, then SiLU(x) = x / (1 + exp(-x))
+ *                or GELU(x) = x * Phi(x) (the exact erf form; "other
+ *                activations" of the norm-fusion companion work).
  *   grouped   -- [P1] "TLX in Production" / "Case Study 3: Distributed
  *                Grouped GEMM for LLM Pretraining": one GEMM per expert over
  *                that expert's rows; written as a loop of plain GEMMs.
@@ -83,11 +85,20 @@ int oracle_num_threads(void)
 #endif
 }
 
-/* Epilogue codes: 0 none, 1 + bias[n], 2 + bias[n] then SiLU. */
+/* GELU(x) = x * Phi(x), Phi(x) = erfc(-x / sqrt(2)) / 2 the standard normal
+ * distribution function (the exact, erf form of GELU). */
+static double gelu(double x)
+{
+    return 0.5 * x * erfc(-x / sqrt(2.0));
+}
+
+/* Epilogue codes: 0 none, 1 + bias[n], 2 + bias[n] then SiLU, 3 + bias[n]
+ * then GELU. */
 static double apply_epilogue(double acc, int epi, const uint16_t *bias_row, int n)
 {
     if (epi >= 1) acc += bf16_to_double(bias_row[n]);
     if (epi == 2) acc = silu(acc);
+    if (epi == 3) acc = gelu(acc);
     return acc;
 }
 

@@ -197,6 +197,37 @@ def test_silu_identities():
     np.testing.assert_allclose(C[0, 0], 0.7310585786300049, rtol=1e-15)
 
 
+def test_gelu_golden_values():
+    pts = np.loadtxt(os.path.join(GOLDEN, "gelu_values.txt"))
+    x = pts[:, 0]
+    A = np.zeros((1, 1))
+    B = np.zeros((x.size, 1))
+    C = oracle.gemm(bf16_bits(A), bf16_bits(B), bias=bf16_bits(x), epi="bias_gelu")
+    np.testing.assert_allclose(C[0], pts[:, 1], rtol=2e-15, atol=1e-17)
+
+
+def test_gelu_identities():
+    # gelu(x) - gelu(-x) = x (since Phi(x) + Phi(-x) = 1); gelu(x) -> x for
+    # large x and -> 0 from below for very negative x; gelu(0) = 0; the
+    # activation acts on bias + A.B^T.
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(64, generator=g) * 3).to(torch.bfloat16)
+    xs = torch.cat([x, -x, torch.tensor([0.0, 40.0, -40.0]).to(torch.bfloat16)])
+    A = np.zeros((1, 1))
+    B = np.zeros((xs.numel(), 1))
+    C = oracle.gemm(bf16_bits(A), bf16_bits(B), bias=xs, epi="bias_gelu")[0]
+    xf = xs.float().numpy().astype(np.float64)
+    n = x.numel()
+    np.testing.assert_allclose(C[:n] - C[n:2 * n], xf[:n], rtol=1e-13, atol=1e-13)
+    assert C[2 * n] == 0.0
+    assert C[2 * n + 1] == 40.0
+    assert -1e-300 <= C[2 * n + 2] <= 0.0
+    A = np.array([[1.0, 2.0]])
+    B = np.array([[1.0, -1.0]])      # s = -1, bias 2 -> gelu(1)
+    C = oracle.gemm(bf16_bits(A), bf16_bits(B), bias=bf16_bits(np.array([2.0])), epi="bias_gelu")
+    np.testing.assert_allclose(C[0, 0], 0.841344746068542948585, rtol=1e-15)
+
+
 # ----------------------------------------------------------------------------
 # grouped GEMM
 # ----------------------------------------------------------------------------
