@@ -81,7 +81,9 @@ typedef enum { WST_F32 = 0, WST_BF16 = 1 } wst_dtype;
 typedef enum {
   WST_EPI_NONE = 0,      /* C = A.B^T                                   */
   WST_EPI_BIAS = 1,      /* C = A.B^T + bias[n]                         */
-  WST_EPI_BIAS_SILU = 2  /* C = SiLU(A.B^T + bias[n]), SiLU(x)=x/(1+e^-x) */
+  WST_EPI_BIAS_SILU = 2, /* C = SiLU(A.B^T + bias[n]), SiLU(x)=x/(1+e^-x) */
+  WST_EPI_BIAS_GELU = 3  /* C = GELU(A.B^T + bias[n]), GELU(x)=x*Phi(x), Phi the standard
+                            normal distribution function (exact erf form) */
 } wst_epilogue;
 
 /* Bytes of workspace a call needs.  GEMM and grouped GEMM need

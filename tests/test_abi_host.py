@@ -64,6 +64,7 @@ def gemm(lib, **kw):
     (dict(ws=None), wst.WST_ERR_INVALID_ARG),
     (dict(lda=32), wst.WST_ERR_INVALID_ARG),
     (dict(epi=7), wst.WST_ERR_INVALID_ARG),
+    (dict(epi=4), wst.WST_ERR_INVALID_ARG),
     (dict(ct=5), wst.WST_ERR_INVALID_ARG),
     (dict(epi=1), wst.WST_ERR_INVALID_ARG),            # bias missing
     (dict(A=FAKE + 8), wst.WST_ERR_ALIGNMENT),

@@ -89,7 +89,7 @@ def test_dense_k_tail_with_nan_padding(wst):
     assert_parity(C, ref, K, amax(d["A"]), amax(d["B"]), False, what="K tail")
 
 
-@pytest.mark.parametrize("epi", ["bias", "bias_silu"])
+@pytest.mark.parametrize("epi", ["bias", "bias_silu", "bias_gelu"])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
 def test_batched_epilogues(wst, epi, out):
     # the skinny recsys batch, scaled down: 6 GEMMs of 300 x 256 x 512
@@ -161,3 +161,12 @@ print("ok")
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("epi", ["bias_silu", "bias_gelu"])
+def test_single_cta_activation_ragged(wst, epi):
+    # M <= 128 runs on single-CTA tiles; N and K ragged
+    d = synthetic.dense(100, 520, 200, seed=1010, bias=True, batch=1)
+    C = dense_run(wst, d["A"], d["B"], torch.float32, bias=d["bias"], epi=epi)
+    ref = oracle.gemm(d["A"], d["B"], bias=d["bias"], epi=epi)
+    assert_parity(C, ref, 200, amax(d["A"]), amax(d["B"]), False, what="single-CTA %s" % epi)

@@ -85,7 +85,8 @@ def test_grouped_all_tokens_one_expert(wst):
     assert_parity(C, ref, 256, amax(d["A"]), amax(d["B"]), True, what="one expert")
 
 
-@pytest.mark.parametrize("epi,out", [("bias", torch.float32), ("bias_silu", torch.bfloat16)])
+@pytest.mark.parametrize("epi,out", [("bias", torch.float32), ("bias_silu", torch.bfloat16),
+                                     ("bias_gelu", torch.bfloat16), ("bias_gelu", torch.float32)])
 def test_grouped_epilogue(wst, epi, out):
     d = synthetic.grouped(experts=6, tokens=500, K=128, N=256, seed=77)
     bias = synthetic._normal(torch.Generator().manual_seed(78), (6, 256), 0.1)

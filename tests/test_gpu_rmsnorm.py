@@ -68,7 +68,8 @@ def test_rmsnorm_shapes(wst, M, N, K, out):
     check(C, d, 1e-6, K)
 
 
-@pytest.mark.parametrize("epi,out", [("bias", torch.float32), ("bias_silu", torch.bfloat16)])
+@pytest.mark.parametrize("epi,out", [("bias", torch.float32), ("bias_silu", torch.bfloat16),
+                                     ("bias_gelu", torch.bfloat16)])
 def test_rmsnorm_batched_epilogue(wst, epi, out):
     d = scaled_rows(300, 256, 512, batch=4, seed=71, bias=True)
     C = run(wst, d, out, 1e-5, epi=epi)

@@ -19,7 +19,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "F32", "BF16",
+    "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "EPI_BIAS_GELU", "F32", "BF16",
     "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
     "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_grouped_gemm_bf16",
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
@@ -31,8 +31,9 @@ __all__ = [
 WST_OK, WST_ERR_INVALID_ARG, WST_ERR_ALIGNMENT, WST_ERR_UNSUPPORTED = 0, 1, 2, 3
 WST_ERR_CUDA, WST_ERR_TIMEOUT, WST_ERR_BAD_OFFSETS = 4, 5, 6
 F32, BF16 = 0, 1
-EPI_NONE, EPI_BIAS, EPI_BIAS_SILU = 0, 1, 2
-_EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_silu": EPI_BIAS_SILU}
+EPI_NONE, EPI_BIAS, EPI_BIAS_SILU, EPI_BIAS_GELU = 0, 1, 2, 3
+_EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_silu": EPI_BIAS_SILU,
+              "bias_gelu": EPI_BIAS_GELU}
 
 _lock = threading.Lock()
 _lib = None

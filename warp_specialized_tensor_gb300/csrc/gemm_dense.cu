@@ -28,9 +28,9 @@ inline int dense_cta_group(int M) {
 
 template <bool OUT_F32, int EPI, int CG, bool NORM>
 int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
-  // 8 epilogue warps for SiLU (exp-heavy), except with the row-statistics
-  // warps, where 4 keep the block at 384 threads.
-  constexpr int EW = (EPI == 2 && !NORM) ? 8 : 4;
+  // 8 epilogue warps for SiLU / GELU (special-function heavy), except with
+  // the row-statistics warps, where 4 keep the block at 384 threads.
+  constexpr int EW = (EPI >= 2 && !NORM) ? 8 : 4;
   constexpr int kStages = stages_for<CG>();
   using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, CG, NORM>;
   auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, CG, NORM>;
@@ -150,13 +150,15 @@ int dispatch(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t s) {
     switch (pr.epi) {
       case 0: return launch_cfg<true, 0, CG, NORM>(pr, dev, s);
       case 1: return launch_cfg<true, 1, CG, NORM>(pr, dev, s);
-      default: return launch_cfg<true, 2, CG, NORM>(pr, dev, s);
+      case 2: return launch_cfg<true, 2, CG, NORM>(pr, dev, s);
+      default: return launch_cfg<true, 3, CG, NORM>(pr, dev, s);
     }
   }
   switch (pr.epi) {
     case 0: return launch_cfg<false, 0, CG, NORM>(pr, dev, s);
     case 1: return launch_cfg<false, 1, CG, NORM>(pr, dev, s);
-    default: return launch_cfg<false, 2, CG, NORM>(pr, dev, s);
+    case 2: return launch_cfg<false, 2, CG, NORM>(pr, dev, s);
+    default: return launch_cfg<false, 3, CG, NORM>(pr, dev, s);
   }
 }
 

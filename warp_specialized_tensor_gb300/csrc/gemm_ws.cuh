@@ -81,6 +81,10 @@ __device__ __forceinline__ Tile dense_tile(const GemmArgs& p, long long t) {
 // --------------------------------------------------------------------------
 // epilogue helpers
 // --------------------------------------------------------------------------
+// GELU(x) = x * Phi(x) (exact erf form; normcdff is the CUDA math library's
+// standard normal distribution function).
+__device__ __forceinline__ float gelu_f(float x) { return x * normcdff(x); }
+
 __device__ __forceinline__ float silu_f(float x) {
   // x * sigmoid(x); __expf overflows to +inf for very negative x, giving -0.
   return __fdividef(x, 1.0f + __expf(-x));
@@ -113,6 +117,10 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat
     if constexpr (EPI == 2) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
+    }
+    if constexpr (EPI == 3) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
     }
   }
 }

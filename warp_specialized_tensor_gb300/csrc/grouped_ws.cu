@@ -113,13 +113,15 @@ int dispatch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t 
     switch (pr.epi) {
       case 0: return launch_grouped<true, 0, CLC>(pr, dev, stream);
       case 1: return launch_grouped<true, 1, CLC>(pr, dev, stream);
-      default: return launch_grouped<true, 2, CLC>(pr, dev, stream);
+      case 2: return launch_grouped<true, 2, CLC>(pr, dev, stream);
+      default: return launch_grouped<true, 3, CLC>(pr, dev, stream);
     }
   }
   switch (pr.epi) {
     case 0: return launch_grouped<false, 0, CLC>(pr, dev, stream);
     case 1: return launch_grouped<false, 1, CLC>(pr, dev, stream);
-    default: return launch_grouped<false, 2, CLC>(pr, dev, stream);
+    case 2: return launch_grouped<false, 2, CLC>(pr, dev, stream);
+    default: return launch_grouped<false, 3, CLC>(pr, dev, stream);
   }
 }
 

@@ -173,6 +173,8 @@ static __device__ __noinline__ void grouped_check_offsets(const GroupedArgs& p) 
 }
 
 __device__ __forceinline__ float grp_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// GELU(x) = x * Phi(x) (exact erf form, the CUDA math library's normcdff).
+__device__ __forceinline__ float grp_gelu(float x) { return x * normcdff(x); }
 
 template <bool OUT_F32, int EPI, bool CLC>
 __global__ void __launch_bounds__(kGrpThreads, 1)
@@ -434,6 +436,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           for (int j = 0; j < 32; ++j) {
             v[j] += bias_v;
             if constexpr (EPI == 2) v[j] = grp_silu(v[j]);
+            if constexpr (EPI == 3) v[j] = grp_gelu(v[j]);
           }
         }
         // Transpose: lane (feature) writes column `lane` of the [token][feature] block.

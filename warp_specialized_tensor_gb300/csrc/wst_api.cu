@@ -205,7 +205,7 @@ wst_status wst_workspace_init(void* workspace, size_t bytes, void* stream) {
 }
 
 static wst_status validate_common(int epi, int c_type, const void* ws) {
-  if (epi < 0 || epi > 2) return fail(WST_ERR_INVALID_ARG, "unknown epilogue %d", epi);
+  if (epi < 0 || epi > 3) return fail(WST_ERR_INVALID_ARG, "unknown epilogue %d", epi);
   if (c_type != WST_F32 && c_type != WST_BF16) return fail(WST_ERR_INVALID_ARG, "unknown c_type %d", c_type);
   if (!ws) return fail(WST_ERR_INVALID_ARG, "workspace is NULL");
   if (!aligned16(ws)) return fail(WST_ERR_ALIGNMENT, "workspace not 16-byte aligned");
