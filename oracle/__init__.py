@@ -58,6 +58,9 @@ def _load():
             lib.oracle_gemm_rmsnorm.argtypes = [I, I, I, I, P, L, L, P, L, L,
                                                 ctypes.c_double, P, L, I, P, L, L, P, I]
             lib.oracle_gemm_rmsnorm.restype = None
+            lib.oracle_gemm_layernorm.argtypes = [I, I, I, I, P, L, L, P, L, L,
+                                                  ctypes.c_double, P, L, I, P, L, L, P, I]
+            lib.oracle_gemm_layernorm.restype = None
             lib.oracle_grouped.argtypes = [I, I, I, I, P, L, P, L, L, P, P, L,
                                            I, P, L]
             lib.oracle_grouped.restype = I
@@ -169,6 +172,35 @@ def gemm_rmsnorm(A, B, eps: float = 1e-6, bias=None, epi: str = "none", rows=Non
         nrows = rows_a.size
     lib.oracle_gemm_rmsnorm(batch, M, N, K, _ptr(a), K, M * K, _ptr(b), K, sB, float(eps),
                             _ptr(bias_a), sBias, code, _ptr(C), N, M * N, _ptr(rows_a), nrows)
+    return C[0] if squeeze else C
+
+
+def gemm_layernorm(A, B, eps: float = 1e-5, bias=None, epi: str = "none", rows=None) -> np.ndarray:
+    """C[b,m,n] = epi(sum_k xhat[b,m,k] B[b,n,k] (+ bias)), xhat the row's
+    LayerNorm (mean and variance over k, two passes).  Conventions as gemm()."""
+    lib = _load()
+    a = _u16(A)
+    b = _u16(B)
+    squeeze = a.ndim == 2
+    if squeeze:
+        a = a[None]
+    batch, M, K = a.shape
+    sB = 0 if b.ndim == 2 else b.shape[1] * b.shape[2]
+    N = b.shape[-2]
+    if b.shape[-1] != K:
+        raise ValueError("K mismatch")
+    code = EPI[epi]
+    bias_a, sBias = None, 0
+    if code:
+        bias_a = _u16(bias)
+        sBias = 0 if bias_a.ndim == 1 else bias_a.shape[-1]
+    C = np.full((batch, M, N), np.nan, dtype=np.float64)
+    rows_a, nrows = None, 0
+    if rows is not None:
+        rows_a = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        nrows = rows_a.size
+    lib.oracle_gemm_layernorm(batch, M, N, K, _ptr(a), K, M * K, _ptr(b), K, sB, float(eps),
+                              _ptr(bias_a), sBias, code, _ptr(C), N, M * N, _ptr(rows_a), nrows)
     return C[0] if squeeze else C
 
 

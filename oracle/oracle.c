@@ -181,6 +181,56 @@ void oracle_gemm_rmsnorm(int batch, int M, int N, int K,
 }
 
 /*
+ * GEMM on LayerNorm-normalised rows of A (same conventions as
+ * oracle_gemm_rmsnorm).  For each row: mu = (1/K) sum_k a[k],
+ * var = (1/K) sum_k (a[k] - mu)^2 (two passes), xhat[k] = (a[k] - mu) /
+ * sqrt(var + eps), then C[n] = epi(sum_k xhat[k] * B[n][k] (+ bias[n])): the
+ * norm's learned scale folded into B and its shift into the bias.
+ */
+void oracle_gemm_layernorm(int batch, int M, int N, int K,
+                           const uint16_t *A, long lda, long sA,
+                           const uint16_t *B, long ldb, long sB, double eps,
+                           const uint16_t *bias, long sBias, int epi,
+                           double *C, long ldc, long sC,
+                           const int *rows, int nrows)
+{
+    long nr = rows ? nrows : M;
+    long total = (long)batch * nr;
+    #pragma omp parallel
+    {
+        double *xh = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (long idx = 0; idx < total; ++idx) {
+            int b = (int)(idx / nr);
+            int m = rows ? rows[idx % nr] : (int)(idx % nr);
+            const uint16_t *a = A + (long)b * sA + (long)m * lda;
+            const uint16_t *bias_row = bias ? bias + (long)b * sBias : 0;
+            double *c = C + (long)b * sC + (long)m * ldc;
+            if (!xh) { for (int n = 0; n < N; ++n) c[n] = NAN; continue; }
+            double mu = 0.0;
+            for (int k = 0; k < K; ++k) mu += bf16_to_double(a[k]);
+            mu /= (double)K;
+            double var = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double d = bf16_to_double(a[k]) - mu;
+                var += d * d;
+            }
+            var /= (double)K;
+            double r = 1.0 / sqrt(var + eps);
+            for (int k = 0; k < K; ++k) xh[k] = (bf16_to_double(a[k]) - mu) * r;
+            for (int n = 0; n < N; ++n) {
+                const uint16_t *bn = B + (long)b * sB + (long)n * ldb;
+                double acc = 0.0;
+                for (int k = 0; k < K; ++k)
+                    acc += xh[k] * bf16_to_double(bn[k]);
+                c[n] = apply_epilogue(acc, epi, bias_row, n);
+            }
+        }
+        free(xh);
+    }
+}
+
+/*
  * Grouped GEMM: group g owns rows [off[g], off[g+1]) of A and C and uses
  * weight matrix B[g] (N x K, K contiguous, at B + g*sBg).  Empty groups
  * contribute nothing.  bias (if epi > 0) is per group: bias + g*sBias.

@@ -391,3 +391,53 @@ def test_rmsnorm_eps_and_epilogue():
     B = small_ints(rng, (4, 8), -2, 2)
     C = oracle.gemm_rmsnorm(bf16_bits(A), bf16_bits(B), eps=1e12)
     np.testing.assert_allclose(C, (A @ B.T) / 1e6, rtol=1e-9, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# GEMM on LayerNorm-normalised rows of A
+# ----------------------------------------------------------------------------
+def test_layernorm_alternating_rows_closed_form():
+    # Row m = c_m + d_m * (+1, -1, +1, -1, ...): mean c_m, variance d_m^2, so
+    # the normalised row is (+-1) * d_m / sqrt(d_m^2 + eps), whatever c_m.
+    K = 16
+    sign = np.where(np.arange(K) % 2 == 0, 1.0, -1.0)
+    c = np.array([0.0, 3.0, -5.0, 100.0])
+    d = np.array([1.0, 2.0, 0.5, 4.0])
+    A = c[:, None] + d[:, None] * sign[None, :]
+    rng = np.random.default_rng(64)
+    B = small_ints(rng, (5, K))
+    for eps in (0.0, 0.25):
+        C = oracle.gemm_layernorm(bf16_bits(A), bf16_bits(B), eps=eps)
+        ref = (d / np.sqrt(d * d + eps))[:, None] * (B @ sign)[None, :]
+        np.testing.assert_allclose(C, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_layernorm_shift_and_scale_invariance():
+    # Adding a constant to a row changes nothing; scaling it by a power of two
+    # changes nothing at eps = 0 (both exact in bf16 for these values).
+    g = torch.Generator().manual_seed(65)
+    A = torch.randint(-8, 9, (6, 32), generator=g).float()
+    B = torch.randn(7, 32, generator=g).to(torch.bfloat16)
+    C1 = oracle.gemm_layernorm(A.to(torch.bfloat16), B, eps=0.0)
+    shift = torch.tensor([0.0, 16.0, -32.0, 64.0, 3.0, -7.0])[:, None]
+    C2 = oracle.gemm_layernorm((A + shift).to(torch.bfloat16), B, eps=0.0)
+    np.testing.assert_allclose(C1, C2, rtol=1e-12, atol=1e-12)
+    scale = torch.tensor([1, 2, 4, 0.5, 8, 0.25])[:, None]
+    C3 = oracle.gemm_layernorm((A * scale).to(torch.bfloat16), B, eps=0.0)
+    np.testing.assert_allclose(C1, C3, rtol=1e-12, atol=1e-12)
+
+
+def test_layernorm_constant_rows_and_zero_mean_rows():
+    # A constant row normalises to zero: the output is exactly the (activated) bias.
+    A = np.full((2, 8), 3.0)
+    B = np.ones((3, 8))
+    bias = np.array([1.0, -2.0, 0.5])
+    C = oracle.gemm_layernorm(bf16_bits(A), bf16_bits(B), eps=1e-5, bias=bf16_bits(bias), epi="bias")
+    assert np.array_equal(C, np.tile(bias, (2, 1)))
+    # Rows with zero mean: LayerNorm is RMSNorm (two independent codings).
+    g = torch.Generator().manual_seed(66)
+    half = torch.randn(4, 12, generator=g)
+    Z = torch.cat([half, -half], dim=1).to(torch.bfloat16)   # each row sums to zero exactly
+    Bz = torch.randn(5, 24, generator=g).to(torch.bfloat16)
+    np.testing.assert_allclose(oracle.gemm_layernorm(Z, Bz, eps=1e-3),
+                               oracle.gemm_rmsnorm(Z, Bz, eps=1e-3), rtol=1e-12, atol=1e-12)
