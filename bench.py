@@ -17,8 +17,9 @@ than L2 (129 MB), so L2 is not flushed between steps.
 sample of the same workload, as the reference arm.
 
 Besides the step, the JSON line carries `parity_workloads`: dense 256^3, the
-skinny batched GEMM, the RMSNorm-fused GEMM and IKBO attention, each timed on
-its own (`--only rmsnorm|attention` times one of the last two alone).
+skinny batched GEMM, the RMSNorm- and LayerNorm-fused GEMMs and IKBO attention,
+each timed on
+its own (`--only rmsnorm|layernorm|attention` times one of them alone).
 """
 from __future__ import annotations
 
@@ -225,7 +226,8 @@ def run_ours(args, rank, world, dist):
     wst.load_library()
     peaks = load_peaks()
 
-    extra_only = {"rmsnorm": "dense8192_rmsnorm", "attention": "ikbo_attention"}.get(args.only)
+    extra_only = {"rmsnorm": "dense8192_rmsnorm", "layernorm": "dense8192_layernorm",
+                  "attention": "ikbo_attention"}.get(args.only)
     if extra_only:
         need = ()
     else:
@@ -478,9 +480,11 @@ def run_ours(args, rank, world, dist):
 def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20, names=None):
     """dense 256^3 (fp32 out; launch-latency bound), the skinny recsys batch
     (512 x 1024x256x512, bias+SiLU, bf16 out; HBM-bound; 940 MB > L2), the
-    row-RMSNorm-fused GEMM on the dense 8192^3 operands, and IKBO attention."""
+    row-RMSNorm- and LayerNorm-fused GEMMs on the dense 8192^3 operands, and
+    IKBO attention."""
     import synthetic
     out = {}
+    extra_ws = [ws]
 
     def dense256():
         d1 = synthetic.workload("dense256")
@@ -506,6 +510,18 @@ def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20, n
         return (lambda: wst.wst_gemm_rmsnorm_bf16(A2, B2, C2, eps=1e-6, workspace=ws, stream=stream),
                 dense_flops(8192, 8192, 8192), dense_bytes(8192, 8192, 8192))
 
+    def dense8192_layernorm():
+        # the fused row-LayerNorm GEMM on the dense 8192^3 operands: the
+        # column-sum kernel and the GEMM, both timed (B read twice)
+        d3 = synthetic.workload("dense8192")
+        A3, B3 = d3["A"].to(dev), d3["B"].to(dev)
+        C3 = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev)
+        ws3 = wst.layernorm_workspace(B3, stream=stream)
+        extra_ws.append(ws3)
+        return (lambda: wst.wst_gemm_layernorm_bf16(A3, B3, C3, eps=1e-5, workspace=ws3,
+                                                    stream=stream),
+                dense_flops(8192, 8192, 8192), dense_bytes(8192, 8192, 8192))
+
     def ikbo_attention():
         # 32 users x 256 candidates x 2 query rows, 4 heads, Dh 128, 2048
         # context rows per user; bf16 out.  FLOPs: QK^T and PV; bytes: Q, the
@@ -522,7 +538,8 @@ def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20, n
                 2 * (2 * nq6 * H6 * Dh6) + 2 * (2 * K6.numel()))
 
     builders = [("dense256", dense256), ("skinny_batch", skinny_batch),
-                ("dense8192_rmsnorm", dense8192_rmsnorm), ("ikbo_attention", ikbo_attention)]
+                ("dense8192_rmsnorm", dense8192_rmsnorm),
+                ("dense8192_layernorm", dense8192_layernorm), ("ikbo_attention", ikbo_attention)]
     for name, build in builders:
         if names is not None and name not in names:
             continue
@@ -544,9 +561,10 @@ def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20, n
                      "gbs": round(by / (ms * 1e-3) / 1e9, 1),
                      "bound": "tensor" if t_flop >= t_byte else "hbm",
                      "frac_roofline": round(max(t_flop, t_byte) / (ms * 1e-3), 4)}
-    st = wst.wst_sync_status(ws, stream)
-    if st != 0:
-        raise RuntimeError("device error in parity workloads: %s" % wst.wst_status_string(st))
+    for w in extra_ws:
+        st = wst.wst_sync_status(w, stream)
+        if st != 0:
+            raise RuntimeError("device error in parity workloads: %s" % wst.wst_status_string(st))
     return out
 
 
@@ -673,9 +691,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the extra workloads (parity cases and next rows)")
-    ap.add_argument("--only", choices=["dense", "grouped", "ikbo", "rmsnorm", "attention"], default=None,
-                    help="time one kernel only (profiling runs); not a bench line. rmsnorm and "
-                         "attention time that extra workload alone")
+    ap.add_argument("--only", choices=["dense", "grouped", "ikbo", "rmsnorm", "layernorm", "attention"],
+                    default=None,
+                    help="time one kernel only (profiling runs); not a bench line. rmsnorm, "
+                         "layernorm and attention time that extra workload alone")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KEY", "REGEX"),

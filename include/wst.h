@@ -124,7 +124,8 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K,
  * Source: the TLX write-up ("How We Built TLX: A Hardware-Native GPU Compiler
  * for Production ML at Scale", companion work on norm fusion into GEMMs, and
  * "Five key areas": model-aware fusion); the pages give no formula, this is
- * the plainest RMSNorm reading.  Runs on single-CTA 128 x 256 tiles.
+ * the plainest RMSNorm reading.  Runs on 256 x 256 CTA-pair tiles when
+ * M > 128, else on single-CTA 128 x 256 tiles.
  */
 wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
                                  const void* A, long lda, long strideA,
@@ -132,6 +133,40 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
                                  const void* bias, long strideBias,
                                  void* C, long ldc, long strideC, wst_dtype c_type,
                                  wst_epilogue epi, void* workspace, void* stream);
+
+/*
+ * GEMM on LayerNorm-normalised rows of A.  Same arguments, layouts and rules
+ * as wst_gemm_rmsnorm_bf16, with
+ *   mu[b][m]   = (1/K) sum_k A[b][m][k]
+ *   var[b][m]  = (1/K) sum_k (A[b][m][k] - mu[b][m])^2      (biased)
+ *   C[b][m][n] = epi( sum_k (A[b][m][k] - mu) / sqrt(var + eps) * B[b][n][k]
+ *                     (+ bias[b][n]) )
+ * i.e. y = LayerNorm(x) W^T (+ b), the norm's per-feature scale folded into B
+ * and its shift into bias by the caller.  Computed as
+ *   r (A.B^T)[m][n] - r mu s[n],   r = 1/sqrt(var + eps),  s[n] = sum_k B[n][k],
+ * so A is still read once: a first kernel writes the column sums s (fp32)
+ * into the workspace, then the GEMM gathers sum_k A and sum_k A^2 from the A
+ * tiles in shared memory (var = E[A^2] - mu^2 in fp32, clamped at 0: rows
+ * whose mean is large against their spread lose precision to cancellation,
+ * ~|mu|^2 / var * 2^-24 relative).
+ * workspace: 16-byte aligned, at least wst_gemm_layernorm_workspace_size(
+ * batch, N, strideB) bytes (workspace_bytes says how many were given;
+ * smaller returns WST_ERR_INVALID_ARG).  Two kernel launches on `stream`.
+ * Source: the same TLX norm-fusion item as wst_gemm_rmsnorm_bf16 (the pages
+ * name LayerNorm and RMSNorm without formulas); standard LayerNorm reading.
+ */
+wst_status wst_gemm_layernorm_bf16(int batch, int M, int N, int K,
+                                   const void* A, long lda, long strideA,
+                                   const void* B, long ldb, long strideB, float eps,
+                                   const void* bias, long strideBias,
+                                   void* C, long ldc, long strideC, wst_dtype c_type,
+                                   wst_epilogue epi, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Workspace bytes wst_gemm_layernorm_bf16 needs: the status header plus
+ * batch (1 when strideB == 0) rows of N fp32 column sums, each padded to a
+ * multiple of 4 floats. */
+size_t wst_gemm_layernorm_workspace_size(int batch, int N, long strideB);
 
 /*
  * Grouped GEMM over G groups sharing N and K.  d_offsets is a DEVICE int32

@@ -121,3 +121,46 @@ def test_ikbo_attention_rejects(lib):
     assert a(*bad) == wst.WST_ERR_ALIGNMENT
     bad = list(args); bad[11] = None
     assert a(*bad) == wst.WST_ERR_INVALID_ARG
+
+
+def test_layernorm_workspace_size(lib):
+    # header + one row of N fp32 sums padded to 4 floats (shared B) ...
+    assert wst.wst_gemm_layernorm_workspace_size(1, 100, 0) == 256 + 100 * 4
+    assert wst.wst_gemm_layernorm_workspace_size(3, 101, 0) == 256 + 104 * 4
+    # ... or one row per batch entry when B has a batch stride
+    assert wst.wst_gemm_layernorm_workspace_size(3, 101, 4096) == 256 + 3 * 104 * 4
+    assert wst.wst_gemm_layernorm_workspace_size(0, 101, 0) == 0
+
+
+def norm_gemm(fn, **kw):
+    a = dict(batch=1, M=128, N=128, K=64, A=FAKE, lda=64, sA=0, B=FAKE, ldb=64, sB=0, eps=1e-5,
+             bias=None, sBias=0, C=FAKE, ldc=128, sC=0, ct=1, epi=0, ws=FAKE, wsb=1 << 20, st=None)
+    a.update(kw)
+    args = [a["batch"], a["M"], a["N"], a["K"], a["A"], a["lda"], a["sA"], a["B"], a["ldb"],
+            a["sB"], a["eps"], a["bias"], a["sBias"], a["C"], a["ldc"], a["sC"], a["ct"],
+            a["epi"], a["ws"]]
+    if fn.__name__ == "wst_gemm_layernorm_bf16":
+        args.append(a["wsb"])
+    return fn(*(args + [a["st"]]))
+
+
+@pytest.mark.parametrize("name", ["wst_gemm_rmsnorm_bf16", "wst_gemm_layernorm_bf16"])
+@pytest.mark.parametrize("kw,code", [
+    (dict(eps=-1.0), wst.WST_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), wst.WST_ERR_INVALID_ARG),
+    (dict(eps=float("inf")), wst.WST_ERR_INVALID_ARG),
+    (dict(N=0), wst.WST_ERR_INVALID_ARG),
+    (dict(epi=2), wst.WST_ERR_INVALID_ARG),            # bias missing
+    (dict(B=FAKE + 8), wst.WST_ERR_ALIGNMENT),
+    (dict(ldb=72, sB=0), wst.WST_ERR_INVALID_ARG),     # not device memory (no GPU here)
+])
+def test_norm_gemm_rejects(lib, name, kw, code):
+    assert norm_gemm(getattr(lib, name), **kw) == code
+
+
+def test_layernorm_rejects_small_workspace(lib):
+    f = lib.wst_gemm_layernorm_bf16
+    assert norm_gemm(f, wsb=256 + 127 * 4) == wst.WST_ERR_INVALID_ARG
+    assert "workspace" in lib.wst_last_error().decode()
+    assert norm_gemm(f, batch=2, sA=8192, sB=8192, sC=16384, wsb=256 + 128 * 4) == wst.WST_ERR_INVALID_ARG
+    assert "workspace" in lib.wst_last_error().decode()

@@ -21,7 +21,8 @@ from . import _build
 __all__ = [
     "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "EPI_BIAS_GELU", "F32", "BF16",
     "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
-    "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_grouped_gemm_bf16",
+    "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_gemm_layernorm_bf16",
+    "wst_gemm_layernorm_workspace_size", "layernorm_workspace", "wst_grouped_gemm_bf16",
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
     "wst_sync_status", "wst_status_string",
     "wst_version",
@@ -71,6 +72,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_gemm_rmsnorm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, ctypes.c_float, P, L,
                                               P, L, L, I, I, P, P]
         lib.wst_gemm_rmsnorm_bf16.restype = I
+        lib.wst_gemm_layernorm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, ctypes.c_float, P,
+                                                L, P, L, L, I, I, P, Z, P]
+        lib.wst_gemm_layernorm_bf16.restype = I
+        lib.wst_gemm_layernorm_workspace_size.argtypes = [I, I, L]
+        lib.wst_gemm_layernorm_workspace_size.restype = Z
         lib.wst_grouped_gemm_bf16.argtypes = [I, I, I, I, P, L, P, L, L, P, P, L, P, L, I, I, P, P]
         lib.wst_grouped_gemm_bf16.restype = I
         lib.wst_ikbo_linear_compress.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
@@ -199,11 +205,7 @@ def wst_gemm_bf16(A, B, C, bias=None, epi="none", workspace=None, stream=None) -
     _check(st, "wst_gemm_bf16")
 
 
-def wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, bias=None, epi="none", workspace=None,
-                          stream=None) -> None:
-    """C[b] = epi(diag(r[b]) . A[b] . B[b]^T (+ bias[b])), r = 1/sqrt(mean(A^2, -1) + eps).
-
-    Same tensor conventions as wst_gemm_bf16."""
+def _norm_gemm_args(A, B, C, bias, epi, workspace):
     _need(A, "A", torch.bfloat16, (2, 3))
     _need(B, "B", torch.bfloat16, (2, 3))
     _need(C, "C", None, (2, 3))
@@ -224,11 +226,49 @@ def wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, bias=None, epi="none", workspace=No
     if e != EPI_NONE:
         _need(bias, "bias", torch.bfloat16, (1, 2))
         sBias = bias.stride(0) if bias.dim() == 2 else 0
+    return batch, M, N, K, sA, sB, sC, e, sBias
+
+
+def wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, bias=None, epi="none", workspace=None,
+                          stream=None) -> None:
+    """C[b] = epi(diag(r[b]) . A[b] . B[b]^T (+ bias[b])), r = 1/sqrt(mean(A^2, -1) + eps).
+
+    Same tensor conventions as wst_gemm_bf16."""
+    batch, M, N, K, sA, sB, sC, e, sBias = _norm_gemm_args(A, B, C, bias, epi, workspace)
     st = load_library().wst_gemm_rmsnorm_bf16(
         batch, M, N, K, A.data_ptr(), A.stride(-2), sA, B.data_ptr(), B.stride(-2), sB,
         float(eps), _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(-2), sC, _ctype(C),
         e, workspace.data_ptr(), _stream_handle(stream))
     _check(st, "wst_gemm_rmsnorm_bf16")
+
+
+def wst_gemm_layernorm_workspace_size(batch: int, N: int, strideB: int = 0) -> int:
+    return int(load_library().wst_gemm_layernorm_workspace_size(batch, N, strideB))
+
+
+def layernorm_workspace(B, device=None, stream=None) -> torch.Tensor:
+    """A zero-filled workspace large enough for wst_gemm_layernorm_bf16 with this B."""
+    batch = B.shape[0] if B.dim() == 3 else 1
+    n = wst_gemm_layernorm_workspace_size(batch, B.shape[-2], B.stride(0) if B.dim() == 3 else 0)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or B.device)
+    wst_workspace_init(ws, stream)
+    return ws
+
+
+def wst_gemm_layernorm_bf16(A, B, C, eps=1e-5, bias=None, epi="none", workspace=None,
+                            stream=None) -> None:
+    """C[b] = epi(LayerNorm(A[b]) . B[b]^T (+ bias[b])), the rows of A normalised
+    to zero mean and unit (biased) variance, eps inside the square root.
+
+    Same tensor conventions as wst_gemm_bf16; the workspace must hold
+    wst_gemm_layernorm_workspace_size(...) bytes (see layernorm_workspace())."""
+    batch, M, N, K, sA, sB, sC, e, sBias = _norm_gemm_args(A, B, C, bias, epi, workspace)
+    st = load_library().wst_gemm_layernorm_bf16(
+        batch, M, N, K, A.data_ptr(), A.stride(-2), sA, B.data_ptr(), B.stride(-2), sB,
+        float(eps), _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(-2), sC, _ctype(C),
+        e, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    _check(st, "wst_gemm_layernorm_bf16")
 
 
 def wst_grouped_gemm_bf16(A, B, offsets, C, bias=None, epi="none", workspace=None,

@@ -26,7 +26,7 @@ inline int dense_cta_group(int M) {
   return M > kBM ? 2 : 1;
 }
 
-template <bool OUT_F32, int EPI, int CG, bool NORM>
+template <bool OUT_F32, int EPI, int CG, int NORM>
 int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
   // 8 epilogue warps for SiLU / GELU (special-function heavy), except with
   // the row-statistics warps, where 4 keep the block at 384 threads.
@@ -91,6 +91,8 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   a.inject_drop_load = take_fault_injection() ? 1 : 0;
   a.eps = pr.eps;
   a.inv_k = 1.0f / (float)pr.K;
+  a.colsum = pr.colsum;
+  a.colsum_stride = pr.colsum_stride;
 
   // Persistent grid: one CTA (pair) per SM (pair) that can be resident.
   long long grid = dev.num_sms;
@@ -144,7 +146,7 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   return ST_OK;
 }
 
-template <int CG, bool NORM>
+template <int CG, int NORM>
 int dispatch(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t s) {
   if (pr.c_f32) {
     switch (pr.epi) {
@@ -166,16 +168,61 @@ int dispatch(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t s) {
 
 int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream);
 
+namespace {
+
+// One warp per row of B: 16-byte vector loads along K (rows start 16-byte
+// aligned: B and its strides are), a scalar tail, then a warp reduction.
+__global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* B, long long ldb,
+                                               long long strideB, int N, int K, int rows,
+                                               float* out) {
+  const int gw = blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+  if (gw >= rows) return;
+  const int b = gw / N, n = gw - b * N;
+  const __nv_bfloat16* row = B + (long long)b * strideB + (long long)n * ldb;
+  float acc = 0.0f;
+  const int kv = K & ~7;
+  for (int k = lane * 8; k < kv; k += 256) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + k));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      acc += f.x + f.y;
+    }
+  }
+  for (int k = kv + lane; k < K; k += 32) acc += __bfloat162float(row[k]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) out[gw] = acc;
+}
+
+}  // namespace
+
+int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
+               cudaStream_t stream) {
+  const long long rows = (long long)nb * N;
+  if (rows > 0x7fffffffLL) {
+    set_error("layernorm: %lld rows of B exceed the column-sum kernel's range", rows);
+    return ST_UNSUPPORTED;
+  }
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  k_colsum<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(B), ldb, strideB, N, K,
+                                     (int)rows, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_colsum");
+  return ST_OK;
+}
+
 int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   DeviceInfo dev;
   int st = current_device_info(&dev);
   if (st) return st;
   if (pr.grouped) return run_gemm_grouped(pr, dev, stream);
-  if (pr.norm)
-    return dense_cta_group(pr.M) == 2 ? dispatch<2, true>(pr, dev, stream)
-                                      : dispatch<1, true>(pr, dev, stream);
-  return dense_cta_group(pr.M) == 2 ? dispatch<2, false>(pr, dev, stream)
-                                    : dispatch<1, false>(pr, dev, stream);
+  const bool pair = dense_cta_group(pr.M) == 2;
+  if (pr.norm == 1) return pair ? dispatch<2, 1>(pr, dev, stream) : dispatch<1, 1>(pr, dev, stream);
+  if (pr.norm == 2) return pair ? dispatch<2, 2>(pr, dev, stream) : dispatch<1, 2>(pr, dev, stream);
+  return pair ? dispatch<2, 0>(pr, dev, stream) : dispatch<1, 0>(pr, dev, stream);
 }
 
 }  // namespace wst

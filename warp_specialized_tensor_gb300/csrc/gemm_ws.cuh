@@ -48,7 +48,9 @@ struct GemmArgs {
   WsHeader* ws;
   unsigned long long timeout_ns;
   int inject_drop_load;   // test hook: CTA 0 skips its first K-block's loads
-  float eps, inv_k;       // row-RMS normalisation (NORM kernels only)
+  float eps, inv_k;       // row normalisation (NORM kernels only)
+  const float* colsum;    // LayerNorm: s[b][n] = sum_k B[b][n][k]
+  long long colsum_stride;
 };
 
 struct Tile {
@@ -125,10 +127,35 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat
   }
 }
 
+// Row normalisation of 32 accumulator columns [col, col+32) of one row:
+// RMSNorm v *= r; LayerNorm v = r*v - (r*mu)*s[n] (s the column sums of B, the
+// same for every row: the warp's lanes read the same addresses).  The sums
+// are read as float4: each batch's row of s is 16-byte aligned and padded to a
+// multiple of 4 floats, and col is a multiple of 32.
+template <int NORM>
+__device__ __forceinline__ void apply_norm(float (&v)[32], float scale, float shift,
+                                           const float* cs, int col, int N) {
+  if constexpr (NORM == 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= scale;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 s = col + j < N ? __ldg(reinterpret_cast<const float4*>(cs + col + j))
+                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      v[j] = fmaf(scale, v[j], -shift * s.x);
+      v[j + 1] = fmaf(scale, v[j + 1], -shift * s.y);
+      v[j + 2] = fmaf(scale, v[j + 2], -shift * s.z);
+      v[j + 3] = fmaf(scale, v[j + 3], -shift * s.w);
+    }
+  }
+}
+
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, bool NORM>
+// NORM: 0 none, 1 RMSNorm, 2 LayerNorm of the rows of A.
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, int NORM>
 struct GemmCfg {
   static constexpr int kStatsWarps = NORM ? 4 : 0;     // row sum-of-squares warps
   static constexpr int kThreads = 128 + 32 * EPI_WARPS + 32 * kStatsWarps;
@@ -138,12 +165,15 @@ struct GemmCfg {
   static constexpr int kBBytes = kBRows * kBK * 2;     // 32 KB (1-CTA) / 16 KB (pair)
   static constexpr int kStageBytes = kABytes + kBBytes;  // per CTA
   static constexpr uint32_t kTxBytes = CG * kStageBytes;  // expected by the leader's full[s]
-  static constexpr int kStageBufs = EPI_WARPS == 4 ? 2 : 1;  // staging buffers per epilogue warp
+  // staging buffers per epilogue warp (one for LayerNorm: its row shifts take
+  // the shared memory of the second)
+  static constexpr int kStageBufs = EPI_WARPS == 4 && NORM != 2 ? 2 : 1;
   static constexpr int kStgBytes = 32 * 128;           // 32 rows x 128 B
   static constexpr int kColsPerChunk = OUT_F32 ? 32 : 64;
   static constexpr int kWarpCols = BN / (EPI_WARPS / 4);  // columns one epilogue warp drains
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kScaleBytes = NORM ? 2 * kBM * 4 : 0;  // per-row scales, 2 buffers
+  // per-row scales (and LayerNorm shifts r*mu), 2 buffers each
+  static constexpr int kScaleBytes = NORM ? (NORM == 2 ? 4 : 2) * kBM * 4 : 0;
   static constexpr size_t kSmemBytes = (size_t)STAGES * kStageBytes +
                                        (size_t)EPI_WARPS * kStageBufs * kStgBytes + kScaleBytes +
                                        256 /*bars*/ + 1024 /*alignment slack*/;
@@ -173,7 +203,7 @@ struct GemmCfg {
 // both CTAs' loads complete on the leader's full[s]; the leader's commits
 // arrive on empty[s] / acc_full[a] in both CTAs; both epilogues arrive on the
 // leader's acc_empty[a]; each CTA drains its own 128 accumulator rows.
-template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, bool NORM>
+template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, int NORM>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     k_gemm_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
@@ -344,7 +374,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
-      float ss = 0.0f;
+      float ss = 0.0f, sm = 0.0f;  // sum of squares, sum (LayerNorm)
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         // the MMAs that read this stage completed (their commit, multicast
         // to both CTAs of a pair, arrives on consumed[s])
@@ -371,6 +401,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
             ss = fmaf(f.x, f.x, ss);
             ss = fmaf(f.y, f.y, ss);
+            if constexpr (NORM == 2) sm += f.x + f.y;
           }
         }
         __syncwarp();
@@ -379,7 +410,15 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       }
       if (!ok) break;
       if (!warp_wait_phase(guard, scle_bar(acc), acc_phase ^ 1u, (kRoleEpilogue << 16) | 0x500 | acc)) break;
-      row_scale[acc * kBM + r] = rsqrtf(ss * p.inv_k + p.eps);
+      if constexpr (NORM == 1) {
+        row_scale[acc * kBM + r] = rsqrtf(ss * p.inv_k + p.eps);
+      } else {
+        // LayerNorm: mean and variance (one pass, fp32; clamped at 0)
+        const float mu = sm * p.inv_k;
+        const float rs = rsqrtf(fmaxf(ss * p.inv_k - mu * mu, 0.0f) + p.eps);
+        row_scale[acc * kBM + r] = rs;
+        row_scale[2 * kBM + acc * kBM + r] = rs * mu;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(sclf_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
@@ -407,12 +446,14 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       const bool full_rows = row_base + 32 <= tl.row_end;
       const __nv_bfloat16* bias_row =
           EPI ? p.bias + (long long)tl.b * p.bias_stride : nullptr;
+      const float* cs_row = NORM == 2 ? p.colsum + (long long)tl.b * p.colsum_stride : nullptr;
       const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      float scale = 1.0f;
+      float scale = 1.0f, shift = 0.0f;
       if constexpr (NORM) {
         if (!warp_wait_phase(guard, sclf_bar(acc), acc_phase, (kRoleEpilogue << 16) | 0x600 | acc)) break;
         (void)mbar_try_wait(sclf_bar(acc), acc_phase);
         scale = row_scale[acc * kBM + q * 32 + (int)lane];
+        if constexpr (NORM == 2) shift = row_scale[2 * kBM + acc * kBM + q * 32 + (int)lane];
         __syncwarp();
         if (lane == 0) mbar_arrive(scle_bar(acc));
       }
@@ -421,19 +462,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       for (int c0 = col_begin; c0 < col_begin + Cfg::kWarpCols; c0 += Cfg::kColsPerChunk) {
         float v0[32];
         tmem_load32(t_lane + c0, v0);
-        if constexpr (NORM) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v0[j] *= scale;
-        }
+        if constexpr (NORM) apply_norm<NORM>(v0, scale, shift, cs_row, tl.n0 + c0, p.N);
         apply_bias_act<EPI>(v0, bias_row, tl.n0 + c0, p.N);
         uint32_t packed[16];
         float v1[32];
         if constexpr (!OUT_F32) {
           tmem_load32(t_lane + c0 + 32, v1);
-          if constexpr (NORM) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v1[j] *= scale;
-          }
+          if constexpr (NORM) apply_norm<NORM>(v1, scale, shift, cs_row, tl.n0 + c0 + 32, p.N);
           apply_bias_act<EPI>(v1, bias_row, tl.n0 + c0 + 32, p.N);
 #pragma unroll
           for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);

@@ -265,13 +265,15 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K, const void* A, long lda
   return (wst_status)run_gemm(p, static_cast<cudaStream_t>(stream));
 }
 
-wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K, const void* A, long lda,
-                                 long strideA, const void* B, long ldb, long strideB, float eps,
-                                 const void* bias, long strideBias, void* C, long ldc,
-                                 long strideC, wst_dtype c_type, wst_epilogue epi,
-                                 void* workspace, void* stream) {
-  g_err[0] = 0;
-  if (!(eps >= 0.0f) || eps > 3.0e38f) return fail(WST_ERR_INVALID_ARG, "eps must be finite and >= 0");
+namespace {
+
+// Validation and problem set-up shared by the normalised-row GEMMs.
+wst_status norm_gemm_problem(const char* what, int batch, int M, int N, int K, const void* A,
+                             long lda, long strideA, const void* B, long ldb, long strideB,
+                             float eps, const void* bias, long strideBias, void* C, long ldc,
+                             long strideC, wst_dtype c_type, wst_epilogue epi, void* workspace,
+                             GemmProblem& p) {
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return fail(WST_ERR_INVALID_ARG, "%s: eps must be finite and >= 0", what);
   wst_status s = validate_common((int)epi, (int)c_type, workspace);
   if (s) return s;
   if (batch < 1 || M < 1 || N < 1 || K < 1)
@@ -296,7 +298,7 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K, const void* A, 
   if (epi) WST_TRY(check_device_ptr(bias, "bias"));
   WST_TRY(check_device_ptr(workspace, "workspace"));
 
-  GemmProblem p{};
+  p = GemmProblem{};
   p.grouped = 0;
   p.batch = batch;
   p.M = M;
@@ -317,9 +319,54 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K, const void* A, 
   p.epi = (int)epi;
   p.offsets = nullptr;
   p.ws = workspace;
-  p.norm = 1;
   p.eps = eps;
+  return WST_OK;
+}
+
+// fp32 column sums of B per batch row, padded to a multiple of 4 floats.
+inline long long colsum_stride(int N) { return ((long long)N + 3) & ~3LL; }
+
+}  // namespace
+
+wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K, const void* A, long lda,
+                                 long strideA, const void* B, long ldb, long strideB, float eps,
+                                 const void* bias, long strideBias, void* C, long ldc,
+                                 long strideC, wst_dtype c_type, wst_epilogue epi,
+                                 void* workspace, void* stream) {
+  g_err[0] = 0;
+  GemmProblem p;
+  WST_TRY(norm_gemm_problem("rmsnorm", batch, M, N, K, A, lda, strideA, B, ldb, strideB, eps,
+                            bias, strideBias, C, ldc, strideC, c_type, epi, workspace, p));
+  p.norm = 1;
   return (wst_status)run_gemm(p, static_cast<cudaStream_t>(stream));
+}
+
+size_t wst_gemm_layernorm_workspace_size(int batch, int N, long strideB) {
+  if (batch < 1 || N < 1 || strideB < 0) return 0;
+  const long long rows = (batch > 1 && strideB != 0) ? batch : 1;
+  return kWsHeaderBytes + (size_t)(rows * colsum_stride(N) * 4);
+}
+
+wst_status wst_gemm_layernorm_bf16(int batch, int M, int N, int K, const void* A, long lda,
+                                   long strideA, const void* B, long ldb, long strideB, float eps,
+                                   const void* bias, long strideBias, void* C, long ldc,
+                                   long strideC, wst_dtype c_type, wst_epilogue epi,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  const size_t need = wst_gemm_layernorm_workspace_size(batch, N, strideB);
+  if (need && workspace_bytes < need)
+    return fail(WST_ERR_INVALID_ARG, "layernorm: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  GemmProblem p;
+  WST_TRY(norm_gemm_problem("layernorm", batch, M, N, K, A, lda, strideA, B, ldb, strideB, eps,
+                            bias, strideBias, C, ldc, strideC, c_type, epi, workspace, p));
+  const int nb = (batch > 1 && strideB != 0) ? batch : 1;
+  float* s = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHeaderBytes);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WST_TRY((wst_status)run_colsum(B, ldb, nb > 1 ? strideB : 0, nb, N, K, s, st));
+  p.norm = 2;
+  p.colsum = s;
+  p.colsum_stride = nb > 1 ? colsum_stride(N) : 0;
+  return (wst_status)run_gemm(p, st);
 }
 
 wst_status wst_grouped_gemm_bf16(int G, int M_total, int N, int K, const void* A, long lda,

@@ -68,8 +68,10 @@ struct GemmProblem {
   int epi;
   const int* offsets;
   void* ws;
-  int norm;    // dense only: scale row m by 1/sqrt(mean_k A[m][k]^2 + eps)
+  int norm;    // dense only: 1 RMSNorm, 2 LayerNorm of the rows of A
   float eps;
+  const float* colsum;        // LayerNorm: column sums of B, [batch][N] (stride 0: shared)
+  long long colsum_stride;
 };
 
 struct IkboProblem {
@@ -97,6 +99,9 @@ struct AttnProblem {
 };
 
 int run_gemm(const GemmProblem& p, cudaStream_t stream);
+// s[b][n] = sum_k B[b][n][k] in fp32 for b < nb (LayerNorm fusion).
+int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
+               cudaStream_t stream);
 int run_ikbo_attention(const AttnProblem& p, cudaStream_t stream);
 int run_ikbo(const IkboProblem& p, cudaStream_t stream);
 int run_ikbo_noalloc(IkboProblem p, int* d_status, cudaStream_t stream);
