@@ -532,8 +532,10 @@ def time_parity_workloads(wst, torch, dev, stream, peaks, ws, iters: int = 20, n
         O6 = torch.empty(Q6.shape, dtype=torch.bfloat16, device=dev)
         nq6, H6, Dh6 = Q6.shape
         Lkv6 = K6.shape[1]
+        ws6 = wst.attention_workspace(device=dev, stream=stream)
+        extra_ws.append(ws6)
         return (lambda: wst.wst_ikbo_attention_bf16(Q6, K6, V6, off6, O6, Lq=d6["Lq"],
-                                                    workspace=ws, stream=stream),
+                                                    workspace=ws6, stream=stream),
                 4.0 * nq6 * Lkv6 * Dh6 * H6,
                 2 * (2 * nq6 * H6 * Dh6) + 2 * (2 * K6.numel()))
 

@@ -264,14 +264,26 @@ wst_status wst_ikbo_linear_compress_noalloc(int num_users, int num_cand, int Du,
  * once per candidate.  The probabilities are rounded to bf16 before the
  * product with V; row maxima, sums and the output accumulate in fp32.
  * This build supports Dh == 128 (else WST_ERR_UNSUPPORTED) and needs
- * num_cand*Lq < 2^31.  `workspace` needs wst_workspace_size(0, 0, 0) bytes
- * (the error word).  Offsets that break the rule are clamped into range on
+ * num_cand*Lq < 2^31.  Offsets that break the rule are clamped into range on
  * the device and latched as WST_ERR_BAD_OFFSETS.
+ * workspace: 16-byte aligned, zero-filled once (wst_workspace_init) and
+ * then reused; `workspace_bytes` says how large it is.  With at least
+ * wst_ikbo_attention_workspace_size() bytes the items (user, head, 128-row
+ * query tile) of the last partial wave of the persistent grid are split by
+ * key blocks over all CTAs and their partial results merged through the
+ * workspace (so the result of a split item is summed in another order);
+ * with less (at least the 256-byte error-word header) whole items only.
+ * One call at a time per workspace.
  */
 wst_status wst_ikbo_attention_bf16(int num_users, int num_cand, int Lq, int H, int Dh, int Lkv,
                                    const void* Q, const void* K, const void* V,
                                    const int* d_user_offsets, float scale,
-                                   void* O, wst_dtype o_type, void* workspace, void* stream);
+                                   void* O, wst_dtype o_type, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for wst_ikbo_attention_bf16's split schedule (header,
+ * per-CTA flags and one partial O/m/l slot per CTA, for up to 256 CTAs). */
+size_t wst_ikbo_attention_workspace_size(void);
 
 /* Synchronize `stream`, then return and clear the first device-side error
  * latched in `workspace` (WST_OK if none). */

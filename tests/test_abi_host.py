@@ -99,8 +99,8 @@ def test_grouped_and_ikbo_reject(lib):
 
 def test_ikbo_attention_rejects(lib):
     a = lib.wst_ikbo_attention_bf16
-    #       users cand Lq H  Dh   Lkv  Q     K     V     off   scale O     type ws    stream
-    args = [32, 8192, 2, 4, 128, 2048, FAKE, FAKE, FAKE, FAKE, 0.088, FAKE, 1, FAKE, None]
+    #       users cand Lq H  Dh   Lkv  Q     K     V     off   scale O     type ws    bytes  stream
+    args = [32, 8192, 2, 4, 128, 2048, FAKE, FAKE, FAKE, FAKE, 0.088, FAKE, 1, FAKE, 1 << 24, None]
     bad = list(args); bad[4] = 64            # Dh != 128
     assert a(*bad) == wst.WST_ERR_UNSUPPORTED
     bad = list(args); bad[5] = 0             # empty context
@@ -121,6 +121,13 @@ def test_ikbo_attention_rejects(lib):
     assert a(*bad) == wst.WST_ERR_ALIGNMENT
     bad = list(args); bad[11] = None
     assert a(*bad) == wst.WST_ERR_INVALID_ARG
+    bad = list(args); bad[14] = 255          # smaller than the error-word header
+    assert a(*bad) == wst.WST_ERR_INVALID_ARG
+
+
+def test_attention_workspace_size(lib):
+    # header + 256 CTAs x 4 flags + 256 slots of O [128][128] fp32, m, l
+    assert wst.wst_ikbo_attention_workspace_size() == 256 + 256 * 16 + 256 * (128 * 128 + 256) * 4
 
 
 def test_layernorm_workspace_size(lib):

@@ -5,7 +5,11 @@ Tolerance, from the kernel's arithmetic: the probabilities are rounded to
 bf16 (relative error <= 2^-9) before the product with V, while the row sums,
 maxima and the output accumulate in fp32, so |O_gpu - O_ref| <= 2^-9 max|V|
 plus fp32 rounding.  The test allows 2^-8 max|V| (a factor 2 of margin),
-plus one bf16 ulp of the reference for bf16 outputs.
+plus one bf16 ulp of the reference for bf16 outputs.  Merging split items
+(the stream-K tail) adds fp32 rounding only.
+
+Every test runs under both schedules: whole items only (a header-only
+workspace) and the split last wave (a full attention workspace).
 """
 import math
 
@@ -27,10 +31,31 @@ def wst():
     return w
 
 
+SCHED = {"sched": "split"}
+
+
+@pytest.fixture(autouse=True, params=["whole", "split"])
+def sched(request):
+    SCHED["sched"] = request.param
+    yield request.param
+
+
+_WS = {}
+
+
+def workspace(wst):
+    # one workspace per schedule, reused across calls (the split schedule's
+    # flags carry a per-call epoch)
+    k = SCHED["sched"]
+    if k not in _WS:
+        _WS[k] = wst.attention_workspace() if k == "split" else wst.workspace()
+    return _WS[k]
+
+
 def run(wst, d, out_dtype=torch.float32, scale=None):
     Q, K, V, off = d["Q"].cuda(), d["K"].cuda(), d["V"].cuda(), d["user_offsets"].cuda()
     O = torch.full(Q.shape, float("nan"), dtype=out_dtype, device="cuda")
-    ws = wst.workspace()
+    ws = workspace(wst)
     wst.wst_ikbo_attention_bf16(Q, K, V, off, O, Lq=d["Lq"], scale=scale, workspace=ws)
     return O, wst.wst_sync_status(ws)
 
@@ -132,3 +157,43 @@ def test_attention_negative_and_zero_scale(wst, scale):
     assert st == 0
     ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 1, scale=scale)
     check(O, ref, d["V"], False, what="scale %g" % scale)
+
+
+def test_attention_one_item_over_many_ctas(wst):
+    # One item of 16 key blocks: under the split schedule each block runs on
+    # its own CTA and the CTA holding block 0 merges 15 partials.
+    d = synthetic.ikbo_attention(users=1, cand_per_user=[10], Lq=3, H=1, Lkv=2000, seed=10)
+    for out in (torch.float32, torch.bfloat16):
+        O, st = run(wst, d, out)
+        assert st == 0
+        ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 3)
+        check(O, ref, d["V"], out == torch.bfloat16, what="one item")
+
+
+def test_attention_one_wave_plus_tail(wst):
+    # SMs + 8 items: one full round-robin wave and a tail of 8 items split
+    # over all CTAs; sampled rows of the first, a middle and the tail items.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_items = sms + 8
+    d = synthetic.ikbo_attention(users=2, cand_per_user=[128 * (n_items // 2), 128 * (n_items - n_items // 2)],
+                                 Lq=1, H=1, Lkv=700, seed=11)
+    O, st = run(wst, d, torch.float32)
+    assert st == 0
+    nq = d["Q"].shape[0]
+    tiles = [0, 1, sms // 2, sms - 1, sms, sms + 3, n_items - 1]
+    cands = sorted({min(nq - 1, 128 * t + r) for t in tiles for r in (0, 77, 127)})
+    ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 1, cands=cands)
+    check(O, ref, d["V"], False, rows=cands, what="wave + tail")
+    assert not torch.isnan(O).any(), "unwritten rows"
+
+
+def test_attention_repeated_calls_same_workspace(wst):
+    # The per-call epoch: back-to-back calls on one workspace with different
+    # inputs must not read each other's partials.
+    d1 = synthetic.ikbo_attention(users=2, cand_per_user=[30, 50], Lq=2, H=2, Lkv=500, seed=12)
+    d2 = synthetic.ikbo_attention(users=2, cand_per_user=[30, 50], Lq=2, H=2, Lkv=500, seed=13)
+    for d in (d1, d2, d1, d2):
+        O, st = run(wst, d, torch.float32)
+        assert st == 0
+        ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 2)
+        check(O, ref, d["V"], False, what="repeat")

@@ -24,6 +24,7 @@ __all__ = [
     "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_gemm_layernorm_bf16",
     "wst_gemm_layernorm_workspace_size", "layernorm_workspace", "wst_grouped_gemm_bf16",
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
+    "wst_ikbo_attention_workspace_size", "attention_workspace",
     "wst_sync_status", "wst_status_string",
     "wst_version",
 ]
@@ -84,8 +85,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_ikbo_linear_compress_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
         lib.wst_ikbo_linear_compress_noalloc.restype = I
         lib.wst_ikbo_attention_bf16.argtypes = [I, I, I, I, I, I, P, P, P, P, ctypes.c_float,
-                                                P, I, P, P]
+                                                P, I, P, Z, P]
         lib.wst_ikbo_attention_bf16.restype = I
+        lib.wst_ikbo_attention_workspace_size.argtypes = []
+        lib.wst_ikbo_attention_workspace_size.restype = Z
         lib.wst_sync_status.argtypes = [P, P]
         lib.wst_sync_status.restype = I
         lib.wst_status_string.argtypes = [I]
@@ -334,7 +337,10 @@ def wst_ikbo_attention_bf16(Q, K, V, user_offsets, O, Lq: int = 1, scale=None, w
 
     Q: bf16 [cand*Lq, H, Dh]; K, V: bf16 [users, Lkv, H, Dh];
     user_offsets: device int32 [users+1] (candidates per user);
-    O: fp32 or bf16 [cand*Lq, H, Dh]; scale defaults to 1/sqrt(Dh)."""
+    O: fp32 or bf16 [cand*Lq, H, Dh]; scale defaults to 1/sqrt(Dh).
+    workspace: attention_workspace() splits the last partial wave of items by
+    key blocks over all SMs; a smaller one (workspace()) schedules whole
+    items only."""
     for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
         _need(t, n, torch.bfloat16, (3,) if n == "Q" else (4,))
         if not t.is_contiguous():
@@ -356,8 +362,20 @@ def wst_ikbo_attention_bf16(Q, K, V, user_offsets, O, Lq: int = 1, scale=None, w
         users, nq // Lq, Lq, H, Dh, Lkv, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
         user_offsets.data_ptr(), float(scale), O.data_ptr(),
         F32 if O.dtype == torch.float32 else BF16, workspace.data_ptr(),
-        _stream_handle(stream))
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "wst_ikbo_attention_bf16")
+
+
+def wst_ikbo_attention_workspace_size() -> int:
+    return int(load_library().wst_ikbo_attention_workspace_size())
+
+
+def attention_workspace(device=None, stream=None) -> torch.Tensor:
+    """A zero-filled workspace for wst_ikbo_attention_bf16's split schedule."""
+    ws = torch.empty(wst_ikbo_attention_workspace_size(), dtype=torch.uint8,
+                     device=device or "cuda")
+    wst_workspace_init(ws, stream)
+    return ws
 
 
 def wst_ikbo_linear_compress_noalloc(U, Cf, W, user_offsets, Y, status=None,

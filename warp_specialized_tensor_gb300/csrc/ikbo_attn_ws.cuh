@@ -41,6 +41,20 @@
 // PV_{j-2} reads (the tensor core runs one thread's MMAs in issue order), so
 // S runs two blocks ahead of PV and the softmax always finds S ready.
 //
+// Schedule: items are dealt round-robin to the persistent CTAs for as many
+// full waves as there are; the items of the last, partial wave are split by
+// key blocks over ALL CTAs ("stream-K": CTA c takes units [lo(c), lo(c+1))
+// of the remaining (item, key block) units, lo(c) = U*c/G).  A CTA that
+// covers an item's later key blocks without its first publishes its
+// un-normalised O, row maxima m and row sums l in the workspace and releases
+// a per-warp flag; the CTA holding the item's first block (processed at the
+// end of its range, after the others published at the start of theirs)
+// merges them with its own:  m* = max m_i,  l* = sum l_i 2^(m_i - m*),
+// O = sum O_i 2^(m_i - m*) / l*.  Flags carry a per-call epoch.  Waits go
+// only from lower to higher CTA indices and the launch is cooperative, so
+// every waited-for CTA is resident.  (With 512 items on 152 SMs the last
+// wave holds 56 items: 84 % wave efficiency without the split.)
+//
 // Roles (256 threads): warp 0 TMA producer (Q once per item into a staging
 // buffer; K_j and V_j per block through separate 3-deep rings, since K_j is
 // consumed two blocks before V_j); warp 1 MMA issuer (one thread); warp 2
@@ -61,12 +75,13 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB: two 64-wide d halves
 constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 32 KB: two 64-wide d halves
 // barriers: q_full, q_empty, qt_full, k_full[S], k_empty[S], v_full[S],
-// v_empty[S], s_full[2], p_full[2], pv_done[2], o_empty
-constexpr int kAttnNumBars = 3 + 4 * kAttnStages + 7;
+// v_empty[S], s_full[2], p_full[2], pv_done[2], o_empty, o_staged,
+// merge_full[4] (one per softmax warp)
+constexpr int kAttnNumBars = 3 + 4 * kAttnStages + 12;
 constexpr size_t kAttnSmemBytes = (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
                                   512 /*barriers*/ + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kAttnNumBars * 8 + 8 <= 512, "barrier area");
+static_assert(kAttnNumBars * 8 + 32 <= 512, "barrier area + TMEM slot, abort flag, epoch, item count");
 // TMEM columns: Q at 0 (64 columns of bf16 pairs), S/P buffers at 64 and
 // 192 (P as bf16 pairs in the first 64 columns of its S buffer), O at 320.
 constexpr int kAttnTmemQ = 0;
@@ -74,6 +89,37 @@ constexpr int kAttnTmemS = 64;
 constexpr int kAttnTmemO = 320;
 static_assert(kAttnTmemO + kAttnDh <= 512, "TMEM columns");
 constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+
+// Stream-K workspace after the 256-byte header: uint32 flags[kAttnMaxCtas][4]
+// (one per softmax warp), then one partial slot per CTA: O as [4 warps][Dh/4
+// column quads][32 rows][4] fp32 (one warp's share is 16 KB contiguous; a
+// thread writes and reads its row's 4 columns as one 16-byte access, a warp
+// 512 contiguous bytes), then m[128], l[128].
+constexpr int kAttnMaxCtas = 256;
+constexpr size_t kAttnFlagsOffset = 256;
+constexpr size_t kAttnSlotsOffset = kAttnFlagsOffset + (size_t)kAttnMaxCtas * 4 * 4;
+constexpr size_t kAttnSlotFloats = (size_t)kAttnDh * kAttnBM + 2 * kAttnBM;
+constexpr size_t kAttnWorkspaceBytes = kAttnSlotsOffset + (size_t)kAttnMaxCtas * kAttnSlotFloats * 4;
+constexpr int kAttnWarpPartBytes = kAttnDh * 32 * 4;        // 16 KB: one warp's O share
+constexpr int kAttnMergeBatch = 3;                           // partials staged per warp at a time
+static_assert(4 * kAttnMergeBatch * kAttnWarpPartBytes <= 2 * kAttnStages * kAttnKBytes,
+              "merge staging fits in the K/V rings");
+
+// Bulk (TMA engine) copy of `bytes` contiguous bytes global -> shared,
+// completing on an mbarrier (both addresses 16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void attn_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Order this thread's earlier generic-proxy accesses (the flag acquires)
+// before its later async-proxy accesses to global memory.
+__device__ __forceinline__ void attn_fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 struct AttnArgs {
   int num_users, num_cand, Lq, H, Lkv;
@@ -83,6 +129,9 @@ struct AttnArgs {
   void* O;               // [num_cand * Lq][H][Dh], fp32 or bf16
   WsHeader* ws;
   unsigned long long timeout_ns;
+  int split;             // 1: split the last partial wave by key blocks (stream-K)
+  uint32_t* flags;       // [kAttnMaxCtas][4]   (split only)
+  float* slots;          // [kAttnMaxCtas][kAttnSlotFloats]
 };
 
 // 4-D TMA tile load (K and V: {Dh, H, Lkv, users}).
@@ -180,6 +229,68 @@ struct AttnWalker {
   }
 };
 
+// One unit of work: key blocks [jb, je) of item `item`.
+struct AttnFrag {
+  long long item;
+  int jb, je;
+};
+
+// The schedule every role walks in the same order: whole items round-robin
+// (t = blockIdx.x, + gridDim.x, ... below n_full), then this CTA's share
+// [u, hi) of the remaining (item, key block) units.
+struct AttnSched {
+  long long n_full, t, u, hi, base, units;
+  int nblk;
+
+  __device__ __forceinline__ void init(long long n_items, int nblk_, bool split) {
+    nblk = nblk_;
+    const long long G = gridDim.x;
+    n_full = split ? (n_items / G) * G : n_items;
+    t = blockIdx.x;
+    base = n_full * nblk;
+    units = (n_items - n_full) * nblk;
+    u = lo(blockIdx.x);
+    hi = lo(blockIdx.x + 1);
+  }
+  // first tail unit of CTA c
+  __device__ __forceinline__ long long lo(long long c) const {
+    return base + units * c / (long long)gridDim.x;
+  }
+  __device__ __forceinline__ bool next(AttnFrag& f) {
+    if (t < n_full) {
+      f.item = t;
+      f.jb = 0;
+      f.je = nblk;
+      t += gridDim.x;
+      return true;
+    }
+    if (u < hi) {
+      f.item = u / nblk;
+      f.jb = (int)(u - f.item * nblk);
+      f.je = (int)min((long long)nblk, hi - f.item * nblk);
+      u = f.item * nblk + f.je;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Items (user, head, 128-row query tile) of the whole call; offsets clamped
+// as the walker clamps them.  One warp.
+__device__ __forceinline__ long long attn_count_items(const AttnArgs& p, uint32_t lane) {
+  long long cnt = 0;
+  for (int u = (int)lane; u < p.num_users; u += 32) {
+    int a = __ldg(p.uoff + u);
+    int b = __ldg(p.uoff + u + 1);
+    a = min(max(a, 0), p.num_cand);
+    b = min(max(b, a), p.num_cand);
+    cnt += ((long long)(b - a) * p.Lq + kAttnBM - 1) / kAttnBM;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  return cnt * p.H;
+}
+
 static __device__ __noinline__ void attn_check_offsets(const AttnArgs& p) {
   bool bad = __ldg(p.uoff) != 0 || __ldg(p.uoff + p.num_users) != p.num_cand;
   int prev = 0;
@@ -191,10 +302,14 @@ static __device__ __noinline__ void attn_check_offsets(const AttnArgs& p) {
   if (bad) latch_error(p.ws, kErrBadOffsets, 3);
 }
 
+// tmO (bf16 output only): O as {Dh, H, rows}, boxes of 64 d x 1 head x 32
+// rows; a softmax warp stores its 32 rows of a full tile through the Q
+// staging buffer (free once the next Q is in TMEM).
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_ikbo_attn_ws(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const AttnArgs p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const AttnArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -204,6 +319,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnStages * kAttnKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint32_t* epoch_s = tmem_slot + 2;                                  // this call's flag value
+  long long* n_items_s = reinterpret_cast<long long*>(tmem_slot + 4);  // 8-byte aligned
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
@@ -219,6 +336,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto pf_bar = [&](int b) { return bar_base + 8u * (5 + 4 * kAttnStages + b); };
   auto pv_bar = [&](int b) { return bar_base + 8u * (7 + 4 * kAttnStages + b); };
   const uint32_t oe_bar = bar_base + 8u * (9 + 4 * kAttnStages);
+  // o_staged: the 4 softmax warps are done with the Q staging buffer for a
+  // fragment's output (their TMA stores have read it); the producer waits
+  // for output k before loading the Q of fragment k + 2 there.
+  const uint32_t os_bar = bar_base + 8u * (10 + 4 * kAttnStages);
+  auto mg_bar = [&](int w) { return bar_base + 8u * (11 + 4 * kAttnStages + w); };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -236,39 +358,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(pv_bar(b), 1);
     }
     mbar_init(oe_bar, 4);
+    mbar_init(os_bar, 4);
+    for (int w4 = 0; w4 < 4; ++w4) mbar_init(mg_bar(w4), 1);
     *abort_flag = 0u;
+    *epoch_s = p.split ? p.ws->epoch + 1u : 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    if (!OUT_F32) tma_prefetch_desc(&tmO);
   }
   if (warp == 2) {
     tmem_alloc<1>(smem_addr(tmem_slot), 512);
     tmem_relinquish<1>();
+  }
+  if (warp == 3) {
+    const long long n = attn_count_items(p, lane);
+    if (lane == 0) *n_items_s = n;
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const Guard guard{p.ws, abort_flag, p.timeout_ns};
-  const long long stride = gridDim.x;
   const int nblk = p.kv_blocks;
+  const long long n_items = *n_items_s;
+  const uint32_t target = *epoch_s;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       AttnWalker w;
       w.init(p);
+      AttnSched sc;
+      sc.init(n_items, nblk, p.split != 0);
+      AttnFrag f;
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0, it = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride, ++it) {
-        const AttnItem x = w.item(t);
+      for (; ok && sc.next(f) && w.seek(p, f.item); ++it) {
+        const AttnItem x = w.item(f.item);
         if (!wait_phase(guard, q_empty, (it & 1u) ^ 1u, (kRoleProducer << 16) | 0x800)) break;
+        if (it >= 2 && !wait_phase(guard, os_bar, (it - 2u) & 1u, (kRoleProducer << 16) | 0x900)) break;
         mbar_arrive_expect_tx(q_full, kAttnQBytes);
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d(smem_addr(sQ + hf * (kAttnQBytes / 2)), &tmQ, q_full, hf * 64, x.h, x.row0);
-        for (int j = 0; j < nblk; ++j) {
+        for (int j = f.jb; j < f.je; ++j) {
           if (!wait_phase(guard, ke_bar(ks), kph ^ 1u, (kRoleProducer << 16) | ks)) {
             ok = false;
             break;
@@ -301,13 +436,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(kAttnBM, kAttnDh, false, true);
       const uint32_t a_q = tmem_base + kAttnTmemQ;
       const uint32_t d_o = tmem_base + kAttnTmemO;
-      AttnWalker w;
-      w.init(p);
+      AttnSched sc;
+      sc.init(n_items, nblk, p.split != 0);
+      AttnFrag f;
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0, it = 0;
-      long long gb = 0;  // blocks before this item (buffer parity)
+      long long gb = 0;  // blocks before this fragment (buffer parity)
       bool ok = true;
-      for (long long t = blockIdx.x; ok && w.seek(p, t); t += stride, ++it) {
+      for (; ok && sc.next(f); ++it) {
+        const int nb = f.je - f.jb;
         if (!wait_phase(guard, qt_full, it & 1u, (kRoleMma << 16) | 0x800)) break;
         tc_fence_after_sync();
         // Step j: PV_{j-2} (if j >= 2), then S_j (if j < nblk).  S_j
@@ -315,7 +452,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // performs this thread's MMAs in issue order, so PV_{j-2} reads P
         // before S_j writes there (and PV_{j-2} waited for the softmax to
         // finish block j-2, so S_{j-2} has been read as well).
-        for (int j = 0; j < nblk + 2 && ok; ++j) {
+        for (int j = 0; j < nb + 2 && ok; ++j) {
           if (j >= 2) {
             const int jj = j - 2;
             const long long g = gb + jj;
@@ -337,7 +474,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             umma_commit(ve_bar(vs));
             if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
           }
-          if (j < nblk) {
+          if (j < nb) {
             if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
             tc_fence_after_sync();
             const int b = (int)((gb + j) & 1);
@@ -354,7 +491,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
           }
         }
-        gb += nblk;
+        gb += nb;
       }
     }
   } else if (warp == 3) {
@@ -397,15 +534,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     };
     AttnWalker w;
     w.init(p);
+    AttnSched sc;
+    sc.init(n_items, nblk, p.split != 0);
+    AttnFrag f;
     long long gb = 0;
     uint32_t it = 0;
-    long long t = blockIdx.x;
-    bool ok = w.seek(p, t) && copy_q(0);
+    bool pending_release = false;  // published a partial, flag not yet released
+    uint32_t mg_phase = 0;         // merge batches this warp has staged
+    auto release_partial = [&]() {
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        st_release_gpu(p.flags + (size_t)blockIdx.x * 4 + q, target);
+      }
+      pending_release = false;
+    };
+    bool ok = sc.next(f) && w.seek(p, f.item) && copy_q(0);
     while (ok) {
-      const AttnItem x = w.item(t);
+      const AttnItem x = w.item(f.item);
+      const int nb = f.je - f.jb;
       float m = -INFINITY, l = 0.0f;
-      for (int j = 0; j < nblk; ++j) {
-        const long long g = gb + j;
+      for (int jr = 0; jr < nb; ++jr) {
+        const int j = f.jb + jr;  // key block within the context
+        const long long g = gb + jr;
         const int b = (int)(g & 1);
         const uint32_t ph = (uint32_t)((g >> 1) & 1);
         if (!warp_wait_phase(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
@@ -437,7 +587,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         else
           ext = fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
         const float mx = ext * cs;
-        if (j == 0) {
+        if (jr == 0) {
           m = mx;  // the first PV product overwrites O: nothing to rescale
         } else {
           const bool grow = mx > m + kAttnRescaleLog2;
@@ -496,50 +646,258 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(pf_bar(b));
+        if (pending_release) release_partial();
       }
       if (!ok) break;
-      // Bring the next item's Q into TMEM before this item's output, so its
-      // first S products overlap the epilogue.  Every S product of this item
-      // (the readers of Q in TMEM) completed before the last s_full above.
-      t += stride;
+      // Bring the next fragment's Q into TMEM before this one's output, so
+      // its first S products overlap the epilogue.  Every S product of this
+      // fragment (the readers of Q in TMEM) completed before the last s_full.
+      AttnFrag fn;
+      const bool more = sc.next(fn) && w.seek(p, fn.item);
       ++it;
-      const bool more = w.seek(p, t);
       if (more && !copy_q(it)) break;
-      // Output: wait for the last PV product, read O, divide by l, store.
-      const long long gl = gb + nblk - 1;
+      // Output: wait for the last PV product, then one of three ends.
+      const long long gl = gb + nb - 1;
       if (!warp_wait_phase(guard, pv_bar((int)(gl & 1)), (uint32_t)((gl >> 1) & 1),
                            (kRoleEpilogue << 16) | 0x300)) { ok = false; break; }
       tc_fence_after_sync();
-      gb += nblk;
-      const float inv = 1.0f / l;
+      gb += nb;
       const bool store = row < x.rows;
       const long long base = ((long long)(x.row0 + row) * p.H + x.h) * kAttnDh;
+      auto store_chunk = [&](int c, float (&v)[32], float inv) {
+        if (!store) return;
+        if constexpr (OUT_F32) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + base + c * 32);
 #pragma unroll
-      for (int c = 0; c < kAttnDh / 32; ++c) {
-        float v[32];
-        tmem_load32(t_o + c * 32, v);
-        if (store) {
-          if constexpr (OUT_F32) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + base + c * 32);
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + base + c * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+        }
+      };
+      // Full bf16 tiles leave through the Q staging buffer and TMA; the
+      // rest (fp32 output, ragged tiles that must not touch the next
+      // user's rows) through direct stores.
+      const bool tma_out = !OUT_F32 && x.rows == kAttnBM;
+      auto emit_chunk = [&](int c, float (&v)[32], float inv) {
+        if (tma_out) {
+          // 32 columns = 64 B of the row, in d-half c/2 at byte (c%2)*64:
+          // 16-byte units (c%2)*4 .. +3, 128-byte swizzle as the Q tile.
+          const uint32_t rb = smem_addr(sQ) + (uint32_t)((c >> 1) * (kAttnQBytes / 2) + row * 128);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t unit = (uint32_t)((c & 1) * 4 + jj);
+            st_shared_v4(rb + ((unit ^ (uint32_t)(row & 7)) << 4),
+                         pack_bf16x2(v[8 * jj] * inv, v[8 * jj + 1] * inv),
+                         pack_bf16x2(v[8 * jj + 2] * inv, v[8 * jj + 3] * inv),
+                         pack_bf16x2(v[8 * jj + 4] * inv, v[8 * jj + 5] * inv),
+                         pack_bf16x2(v[8 * jj + 6] * inv, v[8 * jj + 7] * inv));
+          }
+        } else {
+          store_chunk(c, v, inv);
+        }
+      };
+      bool staged = false;  // this warp's rows wait in the staging buffer
+      if (f.jb != 0) {
+        // Later key blocks of a split item: publish O, m, l for the CTA that
+        // holds the item's first block.
+        float* slot = p.slots + (size_t)blockIdx.x * kAttnSlotFloats;
+        float4* part = reinterpret_cast<float4*>(slot + (size_t)q * (kAttnDh * 32));
+#pragma unroll
+        for (int c = 0; c < kAttnDh / 32; ++c) {
+          float v[32];
+          tmem_load32(t_o + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            __stcg(part + (c * 8 + j) * 32 + lane, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        }
+        __stcg(slot + kAttnDh * kAttnBM + row, m);
+        __stcg(slot + kAttnDh * kAttnBM + kAttnBM + row, l);
+        // __syncwarp orders the lanes' stores before lane 0's GPU-scope
+        // fence and release of the flag (one fence per warp: a fence in
+        // every thread waits for each one's stores under a loaded memory
+        // system).  The release waits until this warp has run the softmax
+        // of the next fragment's first block, when the stores have drained
+        // and the fence no longer stalls (the merging CTA needs the partial
+        // only at the end of its own range).
+        __syncwarp();
+        pending_release = true;
+      } else if (f.je != nblk) {
+        // First key blocks of a split item (always this CTA's last fragment,
+        // so the K/V rings are idle): merge the partials of the CTAs whose
+        // ranges cover the rest of the item, up to kAttnMergeBatch at a time.
+        // Their flags are awaited in parallel (one lane each), their 16 KB
+        // shares copied into this warp's 48 KB of the rings, and the running
+        // (m, l, O) rescaled in TMEM:  m' = max(m, m_k),
+        // l' = l 2^(m - m') + sum l_k 2^(m_k - m'),  O' likewise.
+        const long long item_end = (f.item + 1) * nblk;
+        const uint32_t stg = smem_addr(sK) + (uint32_t)(q * kAttnMergeBatch * kAttnWarpPartBytes);
+        // Walk the CTAs after this one: lo(c) = base + floor(units * c / G)
+        // stepped by the quotient and remainder of units / G (no 64-bit
+        // division per CTA), skipping CTAs whose range is empty.
+        const long long G = gridDim.x;
+        const long long dq = sc.units / G, dr = sc.units % G;
+        long long c2 = (long long)blockIdx.x + 1;
+        long long lo_c = sc.lo(c2), rem = (sc.units * c2) % G;
+        auto next_partial = [&]() -> int {
+          while (c2 < G && lo_c < item_end) {
+            const bool wrap = rem + dr >= G;
+            const long long lo_n = lo_c + dq + (wrap ? 1 : 0);
+            const int c = (int)c2;
+            const bool nonempty = lo_n > lo_c;
+            lo_c = lo_n;
+            rem = wrap ? rem + dr - G : rem + dr;
+            ++c2;
+            if (nonempty) return c;
+          }
+          return -1;
+        };
+        int cs0 = -1, cs1 = -1, cs2 = -1, nbat = 0;
+        auto collect = [&]() {
+          cs0 = next_partial();
+          cs1 = cs0 >= 0 ? next_partial() : -1;
+          cs2 = cs1 >= 0 ? next_partial() : -1;
+          nbat = (cs0 >= 0) + (cs1 >= 0) + (cs2 >= 0);
+        };
+        collect();
+        bool emitted = false;
+        while (nbat > 0) {
+          const int b0 = cs0, b1 = cs1, b2 = cs2, nb0 = nbat;
+          const int mine = lane == 0 ? b0 : (lane == 1 ? b1 : b2);
+          uint32_t got = 1;
+          if ((int)lane < nb0)
+            got = wait_flag(guard, p.flags + (size_t)mine * 4 + q, target, (kRoleEpilogue << 16) | 0x700) ? 1u : 0u;
+          // The waiting lanes' acquires and this warp barrier order the
+          // copies below after the publishers' releases; the copies and the
+          // m, l loads read L2, not this SM's L1.
+          if (!__all_sync(0xffffffffu, got != 0)) { ok = false; break; }
+          if (lane == 0) {
+            // one 16 KB bulk copy per partial (this warp's rows)
+            attn_fence_proxy_async_global();
+            mbar_arrive_expect_tx(mg_bar(q), (uint32_t)(nb0 * kAttnWarpPartBytes));
+#pragma unroll
+            for (int k = 0; k < kAttnMergeBatch; ++k) {
+              const int ck = k == 0 ? b0 : (k == 1 ? b1 : b2);
+              if (k < nb0)
+                attn_bulk_g2s(stg + (uint32_t)(k * kAttnWarpPartBytes),
+                              p.slots + (size_t)ck * kAttnSlotFloats + (size_t)q * (kAttnDh * 32),
+                              (uint32_t)kAttnWarpPartBytes, mg_bar(q));
+            }
+          }
+          float mk[kAttnMergeBatch], lk[kAttnMergeBatch];
+#pragma unroll
+          for (int k = 0; k < kAttnMergeBatch; ++k) {
+            const int ck = k == 0 ? b0 : (k == 1 ? b1 : b2);
+            mk[k] = -INFINITY;
+            lk[k] = 0.0f;
+            if (k < nb0) {
+              const float* sl = p.slots + (size_t)ck * kAttnSlotFloats;
+              mk[k] = __ldcg(sl + kAttnDh * kAttnBM + row);
+              lk[k] = __ldcg(sl + kAttnDh * kAttnBM + kAttnBM + row);
+            }
+          }
+          collect();  // the next batch, while the copies fly
+          const bool last = nbat == 0;
+          if (!warp_wait_phase(guard, mg_bar(q), mg_phase & 1u, (kRoleEpilogue << 16) | 0xA00)) {
+            ok = false;
+            break;
+          }
+          (void)mbar_try_wait(mg_bar(q), mg_phase & 1u);  // each lane acquires the copies
+          ++mg_phase;
+          float mn = m;
+#pragma unroll
+          for (int k = 0; k < kAttnMergeBatch; ++k) mn = fmaxf(mn, mk[k]);
+          const float a_self = attn_ex2(m - mn);
+          float ak[kAttnMergeBatch];
+          l *= a_self;
+#pragma unroll
+          for (int k = 0; k < kAttnMergeBatch; ++k) {
+            ak[k] = k < nb0 ? attn_ex2(mk[k] - mn) : 0.0f;
+            l = fmaf(lk[k], ak[k], l);
+          }
+          m = mn;
+          const float inv = 1.0f / l;
+#pragma unroll 1
+          for (int c = 0; c < kAttnDh / 32; ++c) {
+            float v[32];
+            tmem_load32(t_o + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= a_self;
+#pragma unroll
+            for (int k = 0; k < kAttnMergeBatch; ++k) {
+              if (k < nb0) {
+                const uint32_t src = stg + (uint32_t)(k * kAttnWarpPartBytes + ((c * 8) * 32 + (int)lane) * 16);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  float x0, x1, x2, x3;
+                  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                               : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3)
+                               : "r"(src + (uint32_t)(j * 512)));
+                  v[4 * j] = fmaf(ak[k], x0, v[4 * j]);
+                  v[4 * j + 1] = fmaf(ak[k], x1, v[4 * j + 1]);
+                  v[4 * j + 2] = fmaf(ak[k], x2, v[4 * j + 2]);
+                  v[4 * j + 3] = fmaf(ak[k], x3, v[4 * j + 3]);
+                }
+              }
+            }
+            if (last) emit_chunk(c, v, inv);  // the merged, normalised rows
+            else attn_tmem_store32(t_o + c * 32, v);
+          }
+          if (last) {
+            emitted = true;
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + base + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
-                                  pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
-                                  pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
-                                  pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+            attn_tmem_store_wait();
+            __syncwarp();  // the staging buffers are refilled by the next batch
           }
         }
+        if (!ok) break;
+        if (!emitted) {  // no partial had work (not reached: the item is split)
+          const float inv = 1.0f / l;
+#pragma unroll
+          for (int c = 0; c < kAttnDh / 32; ++c) {
+            float v[32];
+            tmem_load32(t_o + c * 32, v);
+            emit_chunk(c, v, inv);
+          }
+        }
+        staged = tma_out;
+      } else {
+        const float inv = 1.0f / l;
+#pragma unroll
+        for (int c = 0; c < kAttnDh / 32; ++c) {
+          float v[32];
+          tmem_load32(t_o + c * 32, v);
+          emit_chunk(c, v, inv);
+        }
+        staged = tma_out;
       }
+      // O has been read: free it for the next fragment's PV products, then
+      // store the staged rows (if any) and release the staging buffer.
+      if (staged) fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(oe_bar);
+      if (lane == 0) {
+        mbar_arrive(oe_bar);
+        if (staged) {
+          const uint32_t sb = smem_addr(sQ) + (uint32_t)(q * 32 * 128);
+          tma_store_3d(&tmO, sb, 0, x.h, x.row0 + q * 32);
+          tma_store_3d(&tmO, sb + kAttnQBytes / 2, 64, x.h, x.row0 + q * 32);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+        }
+        mbar_arrive(os_bar);
+      }
       if (!more) break;
+      f = fn;
     }
+    if (pending_release) release_partial();
+    if (lane == 0) bulk_wait_group<0>();  // this warp's output stores are complete
   }
 
   tc_fence_before_sync();
@@ -549,6 +907,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   tc_fence_after_sync();
   if (warp == 2) tmem_dealloc<1>(tmem_base, 512);
+  if (p.split && threadIdx.x == 0) {
+    // The last CTA to finish advances the workspace epoch for the next call.
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.ws->done_ctas, 1u);
+    if (prev == gridDim.x - 1) {
+      p.ws->done_ctas = 0u;
+      p.ws->epoch = target;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace wst

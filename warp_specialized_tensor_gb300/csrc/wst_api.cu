@@ -426,8 +426,12 @@ wst_status wst_grouped_gemm_bf16(int G, int M_total, int N, int K, const void* A
 wst_status wst_ikbo_attention_bf16(int num_users, int num_cand, int Lq, int H, int Dh, int Lkv,
                                    const void* Q, const void* K, const void* V,
                                    const int* d_user_offsets, float scale, void* O,
-                                   wst_dtype o_type, void* workspace, void* stream) {
+                                   wst_dtype o_type, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
   g_err[0] = 0;
+  if (workspace_bytes < kWsHeaderBytes)
+    return fail(WST_ERR_INVALID_ARG, "attention: workspace of %zu bytes (at least %zu)",
+                workspace_bytes, kWsHeaderBytes);
   if (num_users < 1 || num_cand < 0 || Lq < 1 || H < 1 || Dh < 1 || Lkv < 1)
     return fail(WST_ERR_INVALID_ARG, "sizes out of range (users=%d cand=%d Lq=%d H=%d Dh=%d Lkv=%d)",
                 num_users, num_cand, Lq, H, Dh, Lkv);
@@ -465,8 +469,11 @@ wst_status wst_ikbo_attention_bf16(int num_users, int num_cand, int Lq, int H, i
   p.O = O;
   p.o_f32 = o_type == WST_F32;
   p.ws = workspace;
+  p.ws_bytes = workspace_bytes;
   return (wst_status)run_ikbo_attention(p, static_cast<cudaStream_t>(stream));
 }
+
+size_t wst_ikbo_attention_workspace_size(void) { return attention_workspace_bytes(); }
 
 wst_status wst_ikbo_linear_compress(int num_users, int num_cand, int Du, int Dc, int D, int O,
                                     const void* U, const void* Cf, const void* W,

@@ -96,6 +96,7 @@ struct AttnProblem {
   void* O;
   bool o_f32;
   void* ws;
+  size_t ws_bytes;
 };
 
 int run_gemm(const GemmProblem& p, cudaStream_t stream);
@@ -103,6 +104,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream);
 int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
                cudaStream_t stream);
 int run_ikbo_attention(const AttnProblem& p, cudaStream_t stream);
+size_t attention_workspace_bytes();
 int run_ikbo(const IkboProblem& p, cudaStream_t stream);
 int run_ikbo_noalloc(IkboProblem p, int* d_status, cudaStream_t stream);
 size_t ikbo_noalloc_capacity();
