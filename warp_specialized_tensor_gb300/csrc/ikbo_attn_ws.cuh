@@ -42,8 +42,8 @@
 // S runs two blocks ahead of PV and the softmax always finds S ready.
 //
 // Schedule: items are dealt round-robin to the persistent CTAs for as many
-// full waves as there are; the items of the last, partial wave are split by
-// key blocks over ALL CTAs ("stream-K": CTA c takes units [lo(c), lo(c+1))
+// full waves as there are; the items of the last, partial wave (when it is
+// at most half full) are split by key blocks over ALL CTAs ("stream-K": CTA c takes units [lo(c), lo(c+1))
 // of the remaining (item, key block) units, lo(c) = U*c/G).  A CTA that
 // covers an item's later key blocks without its first publishes its
 // un-normalised O, row maxima m and row sums l in the workspace and releases
@@ -245,7 +245,10 @@ struct AttnSched {
   __device__ __forceinline__ void init(long long n_items, int nblk_, bool split) {
     nblk = nblk_;
     const long long G = gridDim.x;
-    n_full = split ? (n_items / G) * G : n_items;
+    // Split only a last wave that is at most half full: a fuller one gains
+    // less than its merges cost.
+    const long long tail = n_items % G;
+    n_full = split && 2 * tail <= G ? n_items - tail : n_items;
     t = blockIdx.x;
     base = n_full * nblk;
     units = (n_items - n_full) * nblk;
