@@ -62,6 +62,7 @@ int launch_attn(const AttnProblem& pr, const DeviceInfo& dev, cudaStream_t strea
   a.O = pr.O;
   a.ws = static_cast<WsHeader*>(pr.ws);
   a.timeout_ns = wait_timeout_ns();
+  a.epoch = next_flag_epoch();
 
   // Persistent grid: one CTA per SM.  Without the key-block split, no more
   // CTAs than the items can use (the per-user item counts live on the

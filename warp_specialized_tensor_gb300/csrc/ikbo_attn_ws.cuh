@@ -50,7 +50,7 @@
 // a per-warp flag; the CTA holding the item's first block (processed at the
 // end of its range, after the others published at the start of theirs)
 // merges them with its own:  m* = max m_i,  l* = sum l_i 2^(m_i - m*),
-// O = sum O_i 2^(m_i - m*) / l*.  Flags carry a per-call epoch.  Waits go
+// O = sum O_i 2^(m_i - m*) / l*.  Flags carry a per-call value from the host.  Waits go
 // only from lower to higher CTA indices and the launch is cooperative, so
 // every waited-for CTA is resident.  (With 512 items on 152 SMs the last
 // wave holds 56 items: 84 % wave efficiency without the split.)
@@ -81,7 +81,7 @@ constexpr int kAttnNumBars = 3 + 4 * kAttnStages + 12;
 constexpr size_t kAttnSmemBytes = (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
                                   512 /*barriers*/ + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kAttnNumBars * 8 + 32 <= 512, "barrier area + TMEM slot, abort flag, epoch, item count");
+static_assert(kAttnNumBars * 8 + 32 <= 512, "barrier area + TMEM slot, abort flag, item count");
 // TMEM columns: Q at 0 (64 columns of bf16 pairs), S/P buffers at 64 and
 // 192 (P as bf16 pairs in the first 64 columns of its S buffer), O at 320.
 constexpr int kAttnTmemQ = 0;
@@ -129,6 +129,7 @@ struct AttnArgs {
   void* O;               // [num_cand * Lq][H][Dh], fp32 or bf16
   WsHeader* ws;
   unsigned long long timeout_ns;
+  uint32_t epoch;        // this call's flag value (split only; nonzero, distinct from earlier calls')
   int split;             // 1: split the last partial wave by key blocks (stream-K)
   uint32_t* flags;       // [kAttnMaxCtas][4]   (split only)
   float* slots;          // [kAttnMaxCtas][kAttnSlotFloats]
@@ -322,7 +323,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnStages * kAttnKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  uint32_t* epoch_s = tmem_slot + 2;                                  // this call's flag value
   long long* n_items_s = reinterpret_cast<long long*>(tmem_slot + 4);  // 8-byte aligned
 
   const int warp = threadIdx.x >> 5;
@@ -364,7 +364,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(os_bar, 4);
     for (int w4 = 0; w4 < 4; ++w4) mbar_init(mg_bar(w4), 1);
     *abort_flag = 0u;
-    *epoch_s = p.split ? p.ws->epoch + 1u : 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
@@ -386,7 +385,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const Guard guard{p.ws, abort_flag, p.timeout_ns};
   const int nblk = p.kv_blocks;
   const long long n_items = *n_items_s;
-  const uint32_t target = *epoch_s;
+  const uint32_t target = p.epoch;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -910,16 +909,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   tc_fence_after_sync();
   if (warp == 2) tmem_dealloc<1>(tmem_base, 512);
-  if (p.split && threadIdx.x == 0) {
-    // The last CTA to finish advances the workspace epoch for the next call.
-    __threadfence();
-    const uint32_t prev = atomicAdd(&p.ws->done_ctas, 1u);
-    if (prev == gridDim.x - 1) {
-      p.ws->done_ctas = 0u;
-      p.ws->epoch = target;
-      __threadfence();
-    }
-  }
 }
 
 }  // namespace wst

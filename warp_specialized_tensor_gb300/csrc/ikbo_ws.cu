@@ -40,6 +40,7 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   a.P = reinterpret_cast<float*>(ws + ikbo_partials_offset(pr.num_users));
   a.ws = reinterpret_cast<WsHeader*>(ws);
   a.timeout_ns = wait_timeout_ns();
+  a.epoch = next_flag_epoch();
 
   CUtensorMap tmU, tmC, tmW, tmY;
   {
@@ -173,7 +174,8 @@ int run_ikbo_noalloc(IkboProblem pr, int* d_status, cudaStream_t stream) {
   int st = ikbo_noalloc_scratch(&scratch);
   if (st) return st;
   // The array keeps the previous call's contents: clear the header (error
-  // word, epoch) and the ready flags so this call starts from zero.
+  // word) and the ready flags so this call starts from zero (the flags'
+  // per-call value alone would already tell old flags apart).
   cudaError_t e = cudaMemsetAsync(scratch, 0, ikbo_partials_offset(pr.num_users), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ikbo scratch)");
   pr.ws = scratch;

@@ -59,6 +59,7 @@ struct IkboArgs {
   float* P;            // [num_users][O][D]
   WsHeader* ws;
   unsigned long long timeout_ns;
+  uint32_t epoch;      // this call's flag value (nonzero, distinct from earlier calls')
   // Candidate range of CTA i is [split[i], split[i+1]): contiguous ranges
   // sized on the host so every CTA moves about the same number of bytes.
   int split[kIkboMaxGrid + 1];
@@ -92,7 +93,6 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
   uint32_t* tmem_slot = misc;                       // [0]
   volatile uint32_t* abort_flag = misc + 1;         // [1]
-  uint32_t* epoch_s = misc + 2;                     // [2]
   uint32_t* cnt = misc + 4;                         // [4 .. 4+slots): user-publish counters
 
   const int warp = threadIdx.x >> 5;
@@ -116,7 +116,6 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
     }
     mbar_init(w_bar, 1);
     *abort_flag = 0u;
-    *epoch_s = p.ws->epoch + 1u;
     fence_mbar_init();
     tma_prefetch_desc(&tmU);
     tma_prefetch_desc(&tmC);
@@ -131,7 +130,7 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t target = *epoch_s;
+  const uint32_t target = p.epoch;
   const Guard guard{p.ws, abort_flag, p.timeout_ns};
   const int c_lo = p.split[blockIdx.x];
   const int c_hi = p.split[blockIdx.x + 1];
@@ -338,16 +337,6 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   }
   tc_fence_after_sync();
   if (warp == 2) tmem_dealloc<1>(tmem_base, 512);
-  if (threadIdx.x == 0) {
-    // The last CTA to finish advances the workspace epoch for the next call.
-    __threadfence();
-    const uint32_t prev = atomicAdd(&p.ws->done_ctas, 1u);
-    if (prev == gridDim.x - 1) {
-      p.ws->done_ctas = 0u;
-      p.ws->epoch = target;
-      __threadfence();
-    }
-  }
 }
 
 }  // namespace wst

@@ -47,6 +47,13 @@ int cuda_fail(cudaError_t e, const char* what) {
   return ST_CUDA;
 }
 
+uint32_t next_flag_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  if (e == 0u) e = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;  // skip 0 on wrap
+  return e;
+}
+
 int current_device_info(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

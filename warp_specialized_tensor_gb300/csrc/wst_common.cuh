@@ -18,8 +18,8 @@ enum : uint32_t {
 struct WsHeader {
   uint32_t error;       // first latched device error (0 = none)
   uint32_t error_info;  // where it happened (role << 16 | detail)
-  uint32_t epoch;       // IKBO: flag value published by the last completed call
-  uint32_t done_ctas;   // IKBO: CTAs of the running call that have finished
+  uint32_t reserved0;   // (unused; the flags' per-call value comes from the host)
+  uint32_t reserved1;
   uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");

@@ -33,6 +33,10 @@ struct DeviceInfo {
 int current_device_info(DeviceInfo* out);  // Status
 
 unsigned long long wait_timeout_ns();
+// A fresh nonzero value for the cross-CTA ready flags of one call (IKBO
+// partials, split attention items): a process-wide counter, so flags left in
+// a workspace by earlier calls never equal it (zeroed workspaces hold 0).
+uint32_t next_flag_epoch();
 
 // Test hook for the bounded-wait error path: when the environment variable
 // WST_FAULT_INJECT=drop_load is set, the first dense GEMM launch of the
