@@ -318,8 +318,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                    // [2 halves][128 rows][64 d] staging
-  uint8_t* sK = sQ + kAttnQBytes;                        // [stage][2 halves][64 keys][64 d]
-  uint8_t* sV = sK + kAttnStages * kAttnKBytes;          // [stage][2 halves][64 keys][64 d]
+  uint8_t* sK = sQ + kAttnQBytes;                        // [stage][2 d-halves][128 keys][64 d]
+  uint8_t* sV = sK + kAttnStages * kAttnKBytes;          // [stage][2 d-halves][128 keys][64 d]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnStages * kAttnKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
