@@ -19,7 +19,8 @@ sample of the same workload, as the reference arm.
 Besides the step, the JSON line carries `parity_workloads`: dense 256^3, the
 skinny batched GEMM, the RMSNorm- and LayerNorm-fused GEMMs and IKBO attention,
 each timed on
-its own (`--only rmsnorm|layernorm|attention` times one of them alone).
+its own (`--only rmsnorm|layernorm|attention|skinny|dense256` times one of
+them alone).
 """
 from __future__ import annotations
 
@@ -227,7 +228,8 @@ def run_ours(args, rank, world, dist):
     peaks = load_peaks()
 
     extra_only = {"rmsnorm": "dense8192_rmsnorm", "layernorm": "dense8192_layernorm",
-                  "attention": "ikbo_attention"}.get(args.only)
+                  "attention": "ikbo_attention", "skinny": "skinny_batch",
+                  "dense256": "dense256"}.get(args.only)
     if extra_only:
         need = ()
     else:
@@ -693,10 +695,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the extra workloads (parity cases and next rows)")
-    ap.add_argument("--only", choices=["dense", "grouped", "ikbo", "rmsnorm", "layernorm", "attention"],
+    ap.add_argument("--only", choices=["dense", "grouped", "ikbo", "rmsnorm", "layernorm", "attention",
+                                       "skinny", "dense256"],
                     default=None,
                     help="time one kernel only (profiling runs); not a bench line. rmsnorm, "
-                         "layernorm and attention time that extra workload alone")
+                         "layernorm, attention, skinny and dense256 time that extra workload alone")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KEY", "REGEX"),
