@@ -171,3 +171,19 @@ def test_layernorm_rejects_small_workspace(lib):
     assert "workspace" in lib.wst_last_error().decode()
     assert norm_gemm(f, batch=2, sA=8192, sB=8192, sC=16384, wsb=256 + 128 * 4) == wst.WST_ERR_INVALID_ARG
     assert "workspace" in lib.wst_last_error().decode()
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
+def test_header_is_plain_c_and_cpp(lang, std, tmp_path):
+    # The boundary is a C ABI: include/wst.h must compile on its own as C99
+    # (and as C++) with no warnings.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "wst.h"\nint main(void) { return (int)wst_workspace_size(0, 0, 0) * 0; }\n')
+    r = subprocess.run([cc, "-std=" + std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
