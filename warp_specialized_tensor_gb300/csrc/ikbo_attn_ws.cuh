@@ -152,6 +152,35 @@ __device__ __forceinline__ float attn_ex2(float x) {
   return y;
 }
 
+// Three-input max / min (one instruction for two new scores).
+__device__ __forceinline__ float attn_max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float attn_min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed fp32 pairs: (x0, x1) = (x0 * a + c, x1 * a + c) and
+// (r0, r1) += (y0, y1), each lane rounded as its scalar form.
+__device__ __forceinline__ void attn_fma2(float& x0, float& x1, float a, float c) {
+  uint64_t x, av, cv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(av) : "f"(a));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(x), "l"(av), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x));
+}
+__device__ __forceinline__ void attn_add2(float& r0, float& r1, float y0, float y1) {
+  uint64_t r, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(y0), "f"(y1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(r), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+}
+
 // Store 32 consecutive fp32 columns of this thread's TMEM lane (warp-wide).
 __device__ __forceinline__ void attn_tmem_store32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -576,8 +605,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) e8[i] = pos ? -INFINITY : INFINITY;
         if (kvalid >= kAttnBN) {
+          // scores 2i, 2i+1 go to accumulator i % 8
+          if (pos) {
 #pragma unroll
-          for (int i = 0; i < kAttnBN; ++i) e8[i & 7] = pos ? fmaxf(e8[i & 7], s[i]) : fminf(e8[i & 7], s[i]);
+            for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_max3(e8[i & 7], s[2 * i], s[2 * i + 1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_min3(e8[i & 7], s[2 * i], s[2 * i + 1]);
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < kAttnBN; ++i)
@@ -621,10 +656,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) rs8[i] = 0.0f;
         if (kvalid >= kAttnBN) {
+          // pairs: one packed FFMA and one packed add per two scores; score
+          // e still sums into rs8[e % 8]
 #pragma unroll
-          for (int i = 0; i < kAttnBN; ++i) {
-            s[i] = attn_ex2(fmaf(s[i], cs, -m));
-            rs8[i & 7] += s[i];
+          for (int i = 0; i < kAttnBN / 2; ++i) {
+            attn_fma2(s[2 * i], s[2 * i + 1], cs, -m);
+            s[2 * i] = attn_ex2(s[2 * i]);
+            s[2 * i + 1] = attn_ex2(s[2 * i + 1]);
+            attn_add2(rs8[2 * (i & 3)], rs8[2 * (i & 3) + 1], s[2 * i], s[2 * i + 1]);
           }
         } else {
 #pragma unroll
