@@ -39,21 +39,27 @@
 // tensor rate and the per-block handshakes doubled.)
 // The issuer queues PV_{j-2} and then S_j, which overwrites the buffer
 // PV_{j-2} reads (the tensor core runs one thread's MMAs in issue order), so
-// S runs two blocks ahead of PV and the softmax always finds S ready.
+// S runs two blocks ahead of PV.  The softmax takes full blocks' scores in
+// pairs (three-input max, packed fp32x2 FMA and add): its instruction
+// stream, one warp per SM sub-partition, is what bounds the kernel.
+// Full 128-row tiles with bf16 output leave through the Q staging buffer
+// (free once the next item's Q is in TMEM) and TMA stores; ragged tiles and
+// fp32 output use direct stores.
 //
 // Schedule: items are dealt round-robin to the persistent CTAs for as many
 // full waves as there are; the items of the last, partial wave (when it is
-// at most half full) are split by key blocks over ALL CTAs ("stream-K": CTA c takes units [lo(c), lo(c+1))
-// of the remaining (item, key block) units, lo(c) = U*c/G).  A CTA that
-// covers an item's later key blocks without its first publishes its
-// un-normalised O, row maxima m and row sums l in the workspace and releases
-// a per-warp flag; the CTA holding the item's first block (processed at the
-// end of its range, after the others published at the start of theirs)
-// merges them with its own:  m* = max m_i,  l* = sum l_i 2^(m_i - m*),
-// O = sum O_i 2^(m_i - m*) / l*.  Flags carry a per-call value from the host.  Waits go
-// only from lower to higher CTA indices and the launch is cooperative, so
-// every waited-for CTA is resident.  (With 512 items on 152 SMs the last
-// wave holds 56 items: 84 % wave efficiency without the split.)
+// at most half full) are split by key blocks over ALL CTAs ("stream-K":
+// CTA c takes units [lo(c), lo(c+1)) of the remaining (item, key block)
+// units, lo(c) = U*c/G).  A CTA that covers an item's later key blocks
+// without its first publishes its un-normalised O, row maxima m and row sums
+// l in the workspace and releases a per-warp flag; the CTA holding the
+// item's first block (processed at the end of its range, after the others
+// published at the start of theirs) merges them with its own:
+// m* = max m_i,  l* = sum l_i 2^(m_i - m*),  O = sum O_i 2^(m_i - m*) / l*.
+// Flags carry a per-call value from the host.  Waits go only from lower to
+// higher CTA indices and the launch is cooperative, so every waited-for CTA
+// is resident.  (With 512 items on 152 SMs the last wave holds 56 items:
+// 84 % wave efficiency without the split.)
 //
 // Roles (256 threads): warp 0 TMA producer (Q once per item into a staging
 // buffer; K_j and V_j per block through separate 3-deep rings, since K_j is
