@@ -86,6 +86,35 @@ typedef enum {
                             normal distribution function (exact erf form) */
 } wst_epilogue;
 
+/*
+ * Process-wide tuning options.  They choose between equivalent schedules of
+ * the same computation (the results are bitwise equal); the pages have no
+ * counterpart.  A value applies to every later call on every thread of the
+ * process; set options between calls, not while another thread is calling.
+ *   WST_OPT_GROUPED_SCHEDULE  tile schedule of wst_grouped_gemm_bf16:
+ *                             WST_SCHED_STATIC (default: persistent CTA pairs
+ *                             walk the tiles in a fixed order) or
+ *                             WST_SCHED_CLC (one CTA pair per tile launched,
+ *                             running pairs take unstarted pairs' tiles by
+ *                             hardware cluster launch control).
+ *   WST_OPT_DENSE_CTA_GROUP   tile shape of the dense, batched and
+ *                             norm-fused GEMMs: 0 automatic (default: CTA
+ *                             pairs on 256-row tiles when M > 128, else one
+ *                             CTA per 128-row tile), 1 always one CTA per
+ *                             128-row tile, 2 always CTA pairs.
+ * wst_set_option returns WST_ERR_INVALID_ARG for an unknown option or value.
+ */
+typedef enum {
+  WST_OPT_GROUPED_SCHEDULE = 0,
+  WST_OPT_DENSE_CTA_GROUP = 1
+} wst_option;
+
+typedef enum { WST_SCHED_STATIC = 0, WST_SCHED_CLC = 1 } wst_schedule;
+
+wst_status wst_set_option(wst_option opt, int value);
+/* Current value of an option in *value (WST_ERR_INVALID_ARG if unknown). */
+wst_status wst_get_option(wst_option opt, int* value);
+
 /* Bytes of workspace a call needs.  GEMM and grouped GEMM need
  * wst_workspace_size(0, 0, 0); IKBO needs wst_workspace_size(num_users, O, D). */
 size_t wst_workspace_size(int num_users, int O, int D);
@@ -230,9 +259,12 @@ wst_status wst_ikbo_linear_compress(int num_users, int num_cand, int Du, int Dc,
  *    process exits; wst_workspace_size(num_users, O, D) must not exceed it
  *    (64 users at O = 32, D = 128 need about 1 MiB).  Larger requests return
  *    WST_ERR_INVALID_ARG before anything is enqueued.
- *  - The call allocates and frees nothing.  Its first call on a device looks
- *    up the array's device address (cudaGetSymbolAddress); make that first
- *    call before any stream capture.
+ *  - The call allocates and frees nothing.  Its first call on a device (and
+ *    the first after a cudaDeviceReset, which gives the device a new
+ *    context) looks up the array's device address with cudaGetSymbolAddress
+ *    and caches it for that context; make that first call before any stream
+ *    capture.  If it comes while `stream` is being captured, the call returns
+ *    WST_ERR_UNSUPPORTED and enqueues nothing.
  *  - Every call on a device shares the one array and clears its header and
  *    flags at the start: calls that can overlap on the GPU (other streams,
  *    other host threads) race and must be serialised by the caller.

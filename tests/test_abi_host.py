@@ -187,3 +187,23 @@ def test_header_is_plain_c_and_cpp(lang, std, tmp_path):
     r = subprocess.run([cc, "-std=" + std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_options_set_get_and_reject(lib):
+    # Process-wide schedule options: values round-trip, bad ones are refused
+    # with WST_ERR_INVALID_ARG and leave the option unchanged.  No GPU needed.
+    import warp_specialized_tensor_gb300 as w
+    assert w.wst_get_option(w.OPT_GROUPED_SCHEDULE) == w.SCHED_STATIC
+    assert w.wst_get_option(w.OPT_DENSE_CTA_GROUP) == 0
+    with w.option(w.OPT_GROUPED_SCHEDULE, w.SCHED_CLC):
+        assert w.wst_get_option(w.OPT_GROUPED_SCHEDULE) == w.SCHED_CLC
+    assert w.wst_get_option(w.OPT_GROUPED_SCHEDULE) == w.SCHED_STATIC
+    for cg in (1, 2, 0):
+        w.wst_set_option(w.OPT_DENSE_CTA_GROUP, cg)
+        assert w.wst_get_option(w.OPT_DENSE_CTA_GROUP) == cg
+    assert lib.wst_set_option(w.OPT_DENSE_CTA_GROUP, 3) == 1
+    assert lib.wst_set_option(w.OPT_GROUPED_SCHEDULE, -1) == 1
+    assert lib.wst_set_option(99, 0) == 1
+    assert b"unknown option" in lib.wst_last_error()
+    assert w.wst_get_option(w.OPT_DENSE_CTA_GROUP) == 0
+    assert w.wst_get_option(w.OPT_GROUPED_SCHEDULE) == w.SCHED_STATIC

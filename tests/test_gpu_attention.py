@@ -109,16 +109,18 @@ def test_attention_scale_argument(wst):
 
 
 def test_attention_full_size_sampled(wst):
+    # Every candidate of eight users: the last four users (whose items fill
+    # the persistent grid's partial last wave, split by key blocks over all
+    # CTAs and merged when the workspace allows) and four drawn at random.
     d = synthetic.workload("ikbo_attention")
     O, st = run(wst, d, torch.bfloat16)
     assert st == 0
     off = d["user_offsets"].tolist()
     Lq = d["Lq"]
+    users = len(off) - 1
     g = torch.Generator().manual_seed(5)
-    cands = set()
-    for u in torch.randperm(len(off) - 1, generator=g)[:4].tolist():
-        cands |= {off[u], off[u + 1] - 1, (off[u] + off[u + 1]) // 2, min(off[u] + 64, off[u + 1] - 1)}
-    cands = sorted(cands)
+    pick = set(range(users - 4, users)) | set(torch.randperm(users - 4, generator=g)[:4].tolist())
+    cands = sorted(c for u in pick for c in range(off[u], off[u + 1]))
     ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], Lq, cands=cands)
     rows = [c * Lq + r for c in cands for r in range(Lq)]
     check(O, ref, d["V"], True, rows=rows, what="full size")

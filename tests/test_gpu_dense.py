@@ -109,21 +109,22 @@ def test_batched_shared_operand_and_bias(wst):
     assert_parity(C, ref, 264, amax(d["A"]), amax(B2), True, what="shared B/bias")
 
 
-def test_skinny_batch_full_size_sampled(wst):
+def test_skinny_batch_full_size_every_gemm(wst):
+    # All 512 GEMMs (1024 x 256 x 512, bias + SiLU) element by element.
     d = synthetic.workload("skinny_batch")
     C = dense_run(wst, d["A"], d["B"], torch.bfloat16, bias=d["bias"], epi="bias_silu")
-    g = torch.Generator().manual_seed(5)
-    bsel = torch.randperm(512, generator=g)[:6].tolist()
-    for b in bsel:
-        ref = oracle.gemm(d["A"][b], d["B"][b], bias=d["bias"][b], epi="bias_silu")
-        assert_parity(C[b], ref, 512, amax(d["A"]), amax(d["B"]), True, what="skinny b=%d" % b)
+    ref = oracle.gemm(d["A"], d["B"], bias=d["bias"], epi="bias_silu")
+    assert_parity(C, ref, 512, amax(d["A"]), amax(d["B"]), True, what="skinny batch")
 
 
 def test_dense8192_full_size_sampled_rows(wst):
+    # 512 rows: 16 in every one of the 32 row tiles of 256 (CTA pairs), at
+    # offsets that differ between tiles and cover both CTAs' 128-row halves,
+    # plus the first and last row; all 8192 columns of each.
     d = synthetic.workload("dense8192")
     C = dense_run(wst, d["A"], d["B"], torch.bfloat16)
-    rows = torch.randperm(8192, generator=torch.Generator().manual_seed(2))[:24].sort().values.tolist()
-    rows += [0, 8191, 127, 128]       # tile edges
+    rows = sorted({t * 256 + j * 16 + (t * 5) % 16 for t in range(32) for j in range(16)} |
+                  {0, 8191})
     ref = oracle.gemm(d["A"], d["B"], rows=rows)
     assert_parity(C.cpu()[rows], ref[rows], 8192, amax(d["A"]), amax(d["B"]), True,
                   what="dense8192 rows")
@@ -138,29 +139,17 @@ def test_repeated_calls_same_workspace(wst):
         assert_parity(C, ref, 128, amax(d["A"]), amax(d["B"]), False, what="repeat")
 
 
-def test_dense_single_cta_path_forced(tmp_path):
-    # The 1-CTA tile path for shapes that would otherwise use CTA pairs
-    # (WST_CTA_GROUP is read once per process, hence a child process).
-    import os
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    code = r'''
-import sys, torch
-sys.path.insert(0, %r); sys.path.insert(0, %r)
-import oracle, synthetic
-import warp_specialized_tensor_gb300 as wst
-from gpu_util import amax, assert_parity, dense_run
-d = synthetic.dense(300, 264, 200, batch=3, seed=31, bias=True)
-C = dense_run(wst, d["A"], d["B"], torch.bfloat16, bias=d["bias"], epi="bias_silu")
-ref = oracle.gemm(d["A"], d["B"], bias=d["bias"], epi="bias_silu")
-assert_parity(C, ref, 200, amax(d["A"]), amax(d["B"]), True, what="1-CTA forced")
-print("ok")
-''' % (root, os.path.join(root, "tests"))
-    env = dict(os.environ, WST_CTA_GROUP="1")
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=600)
-    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+@pytest.mark.parametrize("cg", [1, 2])
+def test_dense_cta_group_forced(wst, cg):
+    # The 1-CTA tile path for shapes that would otherwise use CTA pairs, and
+    # the pair path for a shape of at most 128 rows, chosen through the
+    # process-wide option WST_OPT_DENSE_CTA_GROUP.
+    shape = (300, 264, 200) if cg == 1 else (100, 264, 200)
+    d = synthetic.dense(*shape, batch=3, seed=31 + cg, bias=True)
+    with wst.option(wst.OPT_DENSE_CTA_GROUP, cg):
+        C = dense_run(wst, d["A"], d["B"], torch.bfloat16, bias=d["bias"], epi="bias_silu")
+    ref = oracle.gemm(d["A"], d["B"], bias=d["bias"], epi="bias_silu")
+    assert_parity(C, ref, 200, amax(d["A"]), amax(d["B"]), True, what="CTA group %d forced" % cg)
 
 
 @pytest.mark.parametrize("epi", ["bias_silu", "bias_gelu"])

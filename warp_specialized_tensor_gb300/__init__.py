@@ -25,7 +25,8 @@ __all__ = [
     "wst_gemm_layernorm_workspace_size", "layernorm_workspace", "wst_grouped_gemm_bf16",
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
     "wst_ikbo_attention_workspace_size", "attention_workspace",
-    "wst_sync_status", "wst_status_string",
+    "wst_sync_status", "wst_status_string", "wst_set_option", "wst_get_option", "option",
+    "OPT_GROUPED_SCHEDULE", "OPT_DENSE_CTA_GROUP", "SCHED_STATIC", "SCHED_CLC",
     "wst_version",
 ]
 
@@ -34,6 +35,8 @@ WST_OK, WST_ERR_INVALID_ARG, WST_ERR_ALIGNMENT, WST_ERR_UNSUPPORTED = 0, 1, 2, 3
 WST_ERR_CUDA, WST_ERR_TIMEOUT, WST_ERR_BAD_OFFSETS = 4, 5, 6
 F32, BF16 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_BIAS_SILU, EPI_BIAS_GELU = 0, 1, 2, 3
+OPT_GROUPED_SCHEDULE, OPT_DENSE_CTA_GROUP = 0, 1
+SCHED_STATIC, SCHED_CLC = 0, 1
 _EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_silu": EPI_BIAS_SILU,
               "bias_gelu": EPI_BIAS_GELU}
 
@@ -89,6 +92,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_ikbo_attention_bf16.restype = I
         lib.wst_ikbo_attention_workspace_size.argtypes = []
         lib.wst_ikbo_attention_workspace_size.restype = Z
+        lib.wst_set_option.argtypes = [I, I]
+        lib.wst_set_option.restype = I
+        lib.wst_get_option.argtypes = [I, ctypes.POINTER(ctypes.c_int)]
+        lib.wst_get_option.restype = I
         lib.wst_sync_status.argtypes = [P, P]
         lib.wst_sync_status.restype = I
         lib.wst_status_string.argtypes = [I]
@@ -148,6 +155,37 @@ def _need(t, name, dtype=None, dims=None):
         raise ValueError("%s must have %s dimensions" % (name, dims))
     if t.stride(-1) != 1:
         raise ValueError("%s must have a contiguous last dimension" % name)
+
+
+# ----------------------------------------------------------------------------
+# process-wide options
+# ----------------------------------------------------------------------------
+def wst_set_option(opt: int, value: int) -> None:
+    """Set a process-wide tuning option (OPT_GROUPED_SCHEDULE: SCHED_STATIC or
+    SCHED_CLC; OPT_DENSE_CTA_GROUP: 0 automatic, 1 single-CTA tiles, 2 pairs)."""
+    _check(load_library().wst_set_option(int(opt), int(value)), "wst_set_option")
+
+
+def wst_get_option(opt: int) -> int:
+    v = ctypes.c_int(0)
+    _check(load_library().wst_get_option(int(opt), ctypes.byref(v)), "wst_get_option")
+    return int(v.value)
+
+
+class option:
+    """Context manager: set an option for the duration of a block, then restore it."""
+
+    def __init__(self, opt: int, value: int):
+        self.opt, self.value, self.old = opt, value, None
+
+    def __enter__(self):
+        self.old = wst_get_option(self.opt)
+        wst_set_option(self.opt, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        wst_set_option(self.opt, self.old)
+        return False
 
 
 # ----------------------------------------------------------------------------
@@ -316,6 +354,8 @@ def wst_ikbo_linear_compress(U, Cf, W, user_offsets, Y, workspace, stream=None) 
     _need(user_offsets, "user_offsets", torch.int32, (1,))
     if not Y.is_contiguous():
         raise ValueError("Y must be contiguous")
+    if not user_offsets.is_contiguous():
+        raise ValueError("user_offsets must be contiguous")
     users, Du, D = U.shape
     cand, Dc, D2 = Cf.shape
     O, F = W.shape
@@ -391,8 +431,14 @@ def wst_ikbo_linear_compress_noalloc(U, Cf, W, user_offsets, Y, status=None,
             raise ValueError("%s must be contiguous" % n)
     _need(Y, "Y", torch.float32, (3,))
     _need(user_offsets, "user_offsets", torch.int32, (1,))
+    if not Y.is_contiguous():
+        raise ValueError("Y must be contiguous")
+    if not user_offsets.is_contiguous():
+        raise ValueError("user_offsets must be contiguous")
     if status is not None:
         _need(status, "status", torch.int32, (1,))
+        if not status.is_contiguous():
+            raise ValueError("status must be contiguous")
     users, Du, D = U.shape
     cand, Dc, D2 = Cf.shape
     O, F = W.shape

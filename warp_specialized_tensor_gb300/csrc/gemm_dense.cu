@@ -16,12 +16,9 @@ template <int CG>
 constexpr int stages_for() { return CG == 2 ? 6 : 4; }
 
 // CTA-pair tiles for dense problems with more than one 128-row block, unless
-// WST_CTA_GROUP=1|2 forces a choice (tuning runs).
+// the process-wide option WST_OPT_DENSE_CTA_GROUP forces a choice.
 inline int dense_cta_group(int M) {
-  static int forced = [] {
-    const char* s = std::getenv("WST_CTA_GROUP");
-    return s ? std::atoi(s) : 0;
-  }();
+  const int forced = option_value(OPT_DENSE_CTA_GROUP);
   if (forced == 1 || forced == 2) return forced;
   return M > kBM ? 2 : 1;
 }

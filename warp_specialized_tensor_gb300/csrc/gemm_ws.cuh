@@ -26,6 +26,8 @@
 // between consumers).
 #pragma once
 
+#include <type_traits>
+
 #include "wst_common.cuh"
 
 namespace wst {
@@ -374,7 +376,14 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (long long t = cluster_id; ok && t < p.tiles_total; t += num_clusters) {
-      float ss = 0.0f, sm = 0.0f;  // sum of squares, sum (LayerNorm)
+      // RMSNorm: ss = sum a^2.  LayerNorm: sums of d = a - c and d^2 about a
+      // shift c, the row's first element (the "shifted data" one-pass
+      // variance of Chan, Golub and LeVeque, "Algorithms for computing the
+      // sample variance: analysis and recommendations", The American
+      // Statistician 37(3), 1983): var = E[d^2] - E[d]^2 cancels only as
+      // much as (c - mu)^2 / var, which is small because c is a value of the
+      // row, where the unshifted E[a^2] - mu^2 cancels mu^2 / var.
+      float ss = 0.0f, sm = 0.0f, c = 0.0f;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         // the MMAs that read this stage completed (their commit, multicast
         // to both CTAs of a pair, arrives on consumed[s])
@@ -389,21 +398,47 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
         if constexpr (CG == 2) (void)mbar_try_wait_cluster(ready, phase);  // each lane acquires the phase
         else (void)mbar_try_wait(ready, phase);
         const uint32_t row_addr = smem_addr(smA + stage * Cfg::kABytes) + (uint32_t)r * 128u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t w0, w1, w2, w3;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                       : "r"(row_addr + ((uint32_t)(j ^ (r & 7)) << 4)));
-          const uint32_t w[4] = {w0, w1, w2, w3};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-            ss = fmaf(f.x, f.x, ss);
-            ss = fmaf(f.y, f.y, ss);
-            if constexpr (NORM == 2) sm += f.x + f.y;
+        if constexpr (NORM == 2) {
+          if (kb == 0) {
+            // element k = 0 of the row: the first two bytes of logical
+            // 16-byte chunk 0, stored at chunk (0 ^ (r & 7)) by the swizzle
+            uint32_t w;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(row_addr + ((uint32_t)(r & 7) << 4)));
+            c = __bfloat162float(__ushort_as_bfloat16((unsigned short)(w & 0xffffu)));
           }
         }
+        // K positions past K in the last block are zero-filled by the copy;
+        // LayerNorm's shifted sums must skip them (they would add -c and c^2)
+        const int kvalid = p.K - kb * kBK;
+        auto accumulate = [&](auto masked) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(row_addr + ((uint32_t)(j ^ (r & 7)) << 4)));
+            const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+              if constexpr (NORM == 1) {
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+              } else {
+                float dx = f.x - c, dy = f.y - c;
+                if constexpr (decltype(masked)::value) {
+                  if (8 * j + 2 * e >= kvalid) dx = 0.0f;
+                  if (8 * j + 2 * e + 1 >= kvalid) dy = 0.0f;
+                }
+                ss = fmaf(dx, dx, ss);
+                ss = fmaf(dy, dy, ss);
+                sm += dx + dy;
+              }
+            }
+          }
+        };
+        if (NORM == 2 && kvalid < kBK) accumulate(std::true_type{});
+        else                           accumulate(std::false_type{});
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -413,9 +448,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       if constexpr (NORM == 1) {
         row_scale[acc * kBM + r] = rsqrtf(ss * p.inv_k + p.eps);
       } else {
-        // LayerNorm: mean and variance (one pass, fp32; clamped at 0)
-        const float mu = sm * p.inv_k;
-        const float rs = rsqrtf(fmaxf(ss * p.inv_k - mu * mu, 0.0f) + p.eps);
+        // LayerNorm: mean = c + E[d], biased variance = E[d^2] - E[d]^2
+        // (fp32, clamped at 0)
+        const float dm = sm * p.inv_k;
+        const float mu = c + dm;
+        const float rs = rsqrtf(fmaxf(ss * p.inv_k - dm * dm, 0.0f) + p.eps);
         row_scale[acc * kBM + r] = rs;
         row_scale[2 * kBM + acc * kBM + r] = rs * mu;
       }

@@ -1,7 +1,4 @@
 // grouped_ws.cu -- instantiations and launcher of the grouped (MoE) GEMM.
-#include <cstdlib>
-#include <cstring>
-
 #include "grouped_ws.cuh"
 #include "wst_host.h"
 
@@ -9,13 +6,10 @@ namespace wst {
 
 namespace {
 
-// Tile schedule: the static persistent walk unless WST_GROUPED_SCHED=clc
-// selects hardware cluster launch control (read on every call, so one process
-// can time or test both).
-inline bool grouped_use_clc() {
-  const char* s = std::getenv("WST_GROUPED_SCHED");
-  return s != nullptr && std::strcmp(s, "clc") == 0;
-}
+// Tile schedule: the static persistent walk unless the process-wide option
+// WST_OPT_GROUPED_SCHEDULE selects hardware cluster launch control (read on
+// every call).
+inline bool grouped_use_clc() { return option_value(OPT_GROUPED_SCHEDULE) == 1; }
 
 template <bool OUT_F32, int EPI, bool CLC>
 int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {

@@ -138,12 +138,58 @@ static __device__ __align__(256) uint8_t g_ikbo_scratch[kNoAllocScratchBytes];
 
 size_t ikbo_noalloc_capacity() { return kNoAllocScratchBytes; }
 
-// Device address of g_ikbo_scratch on the current device.  The host-side
-// symbol is only a stand-in, so the address is looked up once per device
-// (with that device current) and cached.
-static int ikbo_noalloc_scratch(void** out) {
+// Device address of g_ikbo_scratch in the calling thread's current CUDA
+// context.  The host-side symbol is only a stand-in, so the address is looked
+// up with cudaGetSymbolAddress, with the device current, and cached per
+// device together with the context's unique id (cuCtxGetId): after a
+// cudaDeviceReset the runtime makes a new context with a new id, the module is
+// loaded again, and the stale address is replaced instead of being reused.
+// A lookup may load the module, which is not a stream operation: if it is
+// needed while `stream` is being captured into a graph, the call is refused.
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+struct ScratchCache {
+  unsigned long long ctx_id;
+  void* addr;
+};
+
+int current_context_id(unsigned long long* id) {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  if (!get_current || !get_id) {
+    set_error("cuCtxGetCurrent / cuCtxGetId are not available from the CUDA driver");
+    return ST_CUDA;
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+    *id = 0;  // no context yet: the lookup below creates the primary context
+    return ST_OK;
+  }
+  if (get_id(ctx, id) != CUDA_SUCCESS) {
+    set_error("cuCtxGetId failed");
+    return ST_CUDA;
+  }
+  return ST_OK;
+}
+}  // namespace
+
+static int ikbo_noalloc_scratch(cudaStream_t stream, void** out) {
   static std::mutex mu;
-  static void* addr[64] = {nullptr};
+  static ScratchCache cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -151,14 +197,29 @@ static int ikbo_noalloc_scratch(void** out) {
     set_error("device ordinal %d out of range", dev);
     return ST_UNSUPPORTED;
   }
+  unsigned long long id = 0;
+  int st = current_context_id(&id);
+  if (st) return st;
   std::lock_guard<std::mutex> lk(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_ikbo_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(ikbo scratch)");
-    addr[dev] = p;
+  if (id != 0 && cache[dev].addr && cache[dev].ctx_id == id) {
+    *out = cache[dev].addr;
+    return ST_OK;
   }
-  *out = addr[dev];
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone) {
+    set_error("ikbo (allocation-free): the first call in a CUDA context looks up the scratch "
+              "array's device address and must not run while the stream is being captured; "
+              "make one call before capturing");
+    return ST_UNSUPPORTED;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_ikbo_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(ikbo scratch)");
+  if (id == 0 && (st = current_context_id(&id))) return st;
+  cache[dev] = ScratchCache{id, p};
+  *out = p;
   return ST_OK;
 }
 
@@ -171,7 +232,7 @@ int run_ikbo_noalloc(IkboProblem pr, int* d_status, cudaStream_t stream) {
     return ST_INVALID_ARG;
   }
   void* scratch = nullptr;
-  int st = ikbo_noalloc_scratch(&scratch);
+  int st = ikbo_noalloc_scratch(stream, &scratch);
   if (st) return st;
   // The array keeps the previous call's contents: clear the header (error
   // word) and the ready flags so this call starts from zero (the flags'

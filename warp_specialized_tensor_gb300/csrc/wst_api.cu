@@ -81,6 +81,14 @@ int current_device_info(DeviceInfo* out) {
   return ST_OK;
 }
 
+namespace {
+std::atomic<int> g_options[OPT_COUNT];  // zero-initialised: every option's default is 0
+}  // namespace
+
+int option_value(int opt) {
+  return (opt >= 0 && opt < OPT_COUNT) ? g_options[opt].load(std::memory_order_relaxed) : 0;
+}
+
 unsigned long long wait_timeout_ns() {
   static unsigned long long v = [] {
     const char* s = std::getenv("WST_TIMEOUT_MS");
@@ -605,6 +613,28 @@ const char* wst_status_string(wst_status s) {
     case WST_ERR_BAD_OFFSETS: return "WST_ERR_BAD_OFFSETS: device offsets are inconsistent";
   }
   return "unknown wst_status";
+}
+
+wst_status wst_set_option(wst_option opt, int value) {
+  g_err[0] = 0;
+  int hi;
+  switch ((int)opt) {
+    case OPT_GROUPED_SCHEDULE: hi = 1; break;
+    case OPT_DENSE_CTA_GROUP: hi = 2; break;
+    default: return fail(WST_ERR_INVALID_ARG, "unknown option %d", (int)opt);
+  }
+  if (value < 0 || value > hi)
+    return fail(WST_ERR_INVALID_ARG, "option %d: value %d outside [0, %d]", (int)opt, value, hi);
+  g_options[(int)opt].store(value, std::memory_order_relaxed);
+  return WST_OK;
+}
+
+wst_status wst_get_option(wst_option opt, int* value) {
+  g_err[0] = 0;
+  if (!value) return fail(WST_ERR_INVALID_ARG, "value is NULL");
+  if ((int)opt < 0 || (int)opt >= OPT_COUNT) return fail(WST_ERR_INVALID_ARG, "unknown option %d", (int)opt);
+  *value = g_options[(int)opt].load(std::memory_order_relaxed);
+  return WST_OK;
 }
 
 const char* wst_last_error(void) { return g_err; }

@@ -32,6 +32,10 @@ struct DeviceInfo {
 };
 int current_device_info(DeviceInfo* out);  // Status
 
+// Process-wide tuning options (wst_option in include/wst.h).
+enum Option : int { OPT_GROUPED_SCHEDULE = 0, OPT_DENSE_CTA_GROUP = 1, OPT_COUNT = 2 };
+int option_value(int opt);
+
 unsigned long long wait_timeout_ns();
 // A fresh nonzero value for the cross-CTA ready flags of one call (IKBO
 // partials, split attention items): a process-wide counter, so flags left in
