@@ -15,7 +15,7 @@ template <bool OUT_F32, int EPI, bool CLC>
 int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
   auto kern = k_grouped_ws<OUT_F32, EPI, CLC>;
   int st;
-  CUtensorMap tmW, tmX;
+  CUtensorMap tmW, tmX, tmXt, tmC;
   GroupedArgs a{};
   a.w_shared = (pr.strideB == 0) ? 1 : 0;
   {
@@ -29,12 +29,28 @@ int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t st
       return st;
   }
   {
-    // token rows of A, K contiguous: {K, M_total}, 32-row boxes
+    // token rows of A, K contiguous: {K, M_total}; 128-row boxes, and
+    // 16-row boxes for thin tiles
     uint64_t dims[2] = {(uint64_t)pr.K, (uint64_t)pr.M};
     uint64_t str[1] = {(uint64_t)pr.lda * 2};
     uint32_t box[2] = {64, (uint32_t)kGrpXBoxRows};
     if ((st = encode_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.A, dims, str, box,
                          CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+    box[1] = (uint32_t)kGrpXThinRows;
+    if ((st = encode_map(&tmXt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.A, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    // C rows (tokens) x features, row-major: {N, M_total}; box = one
+    // epilogue warp's transposed block of 32 features x 32 tokens
+    const uint64_t es = OUT_F32 ? 4 : 2;
+    uint64_t dims[2] = {(uint64_t)pr.N, (uint64_t)pr.M};
+    uint64_t str[1] = {(uint64_t)pr.ldc * es};
+    uint32_t box[2] = {32, 32};
+    if ((st = encode_map(&tmC, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, pr.C, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE)))
       return st;
   }
   a.G = pr.batch;
@@ -92,7 +108,7 @@ int launch_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t st
     pairs = mc;
   }
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a);
+  e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, tmXt, tmC, a);
   if (e != cudaSuccess) return cuda_fail(e, "launch k_grouped_ws");
   return ST_OK;
 }

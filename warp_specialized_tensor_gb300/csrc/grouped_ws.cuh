@@ -27,10 +27,12 @@
 //   warp 3     lane 1 of CTA 0 validates the offsets; with the
 //              cluster-launch-control schedule, lane 0 is the tile scheduler.
 //   warps 4-7  epilogue: each warp drains its 32 feature lanes, 32 tokens at a
-//              time, adds bias / SiLU, transposes through a private shared
-//              buffer and writes whole 64-byte (bf16) / 128-byte (fp32) row
-//              segments of C with masked vector stores, so rows past the
-//              group end (the next expert's tokens) are never touched.
+//              time, adds bias / SiLU / GELU and transposes through a private
+//              double-buffered shared block; blocks of 32 tokens inside the
+//              group leave through TMA stores, the group's last partial block
+//              through masked vector stores of whole 64-byte (bf16) /
+//              128-byte (fp32) row segments, so rows past the group end (the
+//              next expert's tokens) are never touched.
 //
 // "How We Built TLX: A Hardware-Native GPU Compiler for Production ML at
 // Scale" (Meta Engineering): "TLX in Production" and "Case Study 3:
@@ -66,10 +68,20 @@ constexpr int kGrpXBytes = 128 * kGrpBK * 2;   // up to 128 token rows per CTA
 constexpr int kGrpTQ = 2;  // tile-queue slots
 constexpr int kGrpXBoxRows = 128;              // token rows per TMA box (one box per CTA)
 constexpr int kGrpXBoxBytes = kGrpXBoxRows * kGrpBK * 2;
+// Thin token tiles (a group's remainder, at most 128 tokens: at most 64 rows
+// per CTA) load only the rows they use, in 16-row boxes: their K loop is
+// bound by the bytes each K-block moves, and a full 128-row token box would
+// double them (measured on GB300: a thin tile costs its pair ~10 us, about
+// half of a full tile, almost all of it streaming bytes it does not use).
+constexpr int kGrpXThinRows = 16;
+constexpr int kGrpXThinBytes = kGrpXThinRows * kGrpBK * 2;
+constexpr int kGrpThinMaxRows = 64;            // per CTA
 constexpr int kGrpStageBytes = kGrpWBytes + kGrpXBytes;
 constexpr int kGrpStgBytes = 32 * 32 * 4;      // per-warp transpose buffer (fp32 worst case)
+constexpr int kGrpStgBufs = 2;                 // double-buffered for the TMA stores
 constexpr size_t kGrpSmemBytes = (size_t)kGrpStages * kGrpStageBytes +
-                                 (size_t)kGrpEpiWarps * kGrpStgBytes + 512 /*barriers, queue*/ + 1024;
+                                 (size_t)kGrpEpiWarps * kGrpStgBufs * kGrpStgBytes +
+                                 512 /*barriers, queue*/ + 1024;
 static_assert(kGrpSmemBytes <= 232448, "shared memory per CTA");
 
 struct GroupedArgs {
@@ -179,6 +191,7 @@ __device__ __forceinline__ float grp_gelu(float x) { return x * normcdff(x); }
 template <bool OUT_F32, int EPI, bool CLC>
 __global__ void __launch_bounds__(kGrpThreads, 1)
     k_grouped_ws(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const __grid_constant__ CUtensorMap tmXt, const __grid_constant__ CUtensorMap tmC,
                  const GroupedArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -186,7 +199,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   uint8_t* smW = smem;
   uint8_t* smX = smW + kGrpStages * kGrpWBytes;
   uint8_t* smStg = smX + kGrpStages * kGrpXBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smStg + kGrpEpiWarps * kGrpStgBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smStg + kGrpEpiWarps * kGrpStgBufs * kGrpStgBytes);
   // bars: full[S] | empty[S] | acc_full[2] | acc_empty[2] | tq_full[TQ] | tq_empty[TQ]
   //       | clc_full | clc_empty; then the 16-byte cancel response
   constexpr int kNumBars = 2 * kGrpStages + 4 + 2 * kGrpTQ + 2;
@@ -243,6 +256,8 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmXt);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 2) {
     tmem_alloc<2>(smem_addr(tmem_slot), 512);
@@ -290,8 +305,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const GrpTile tl = gw.tile(p, t);
         const int w_row = tl.n0 + (int)rank * 128;
         const int x_row = tl.t0 + (int)rank * (tl.nmma >> 1);
-        const int x_boxes = ((tl.nmma >> 1) + kGrpXBoxRows - 1) / kGrpXBoxRows;
-        const uint32_t tx = 2u * (uint32_t)(kGrpWBytes + x_boxes * kGrpXBoxBytes);
+        const int x_rows = tl.nmma >> 1;  // token rows this CTA holds
+        const bool thin = x_rows <= kGrpThinMaxRows;
+        const int x_boxes = thin ? (x_rows + kGrpXThinRows - 1) / kGrpXThinRows
+                                 : (x_rows + kGrpXBoxRows - 1) / kGrpXBoxRows;
+        const uint32_t tx = 2u * (uint32_t)(kGrpWBytes + x_boxes * (thin ? kGrpXThinBytes : kGrpXBoxBytes));
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase_cluster(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
             ok = false;
@@ -303,8 +321,13 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           tma_load_3d_pair(smem_addr(smW + stage * kGrpWBytes), &tmW, fb, kx, w_row,
                            p.w_shared ? 0 : tl.g);
           const uint32_t xdst = smem_addr(smX + stage * kGrpXBytes);
-          for (int i = 0; i < x_boxes; ++i)
-            tma_load_2d_pair(xdst + i * kGrpXBoxBytes, &tmX, fb, kx, x_row + i * kGrpXBoxRows);
+          if (thin) {
+            for (int i = 0; i < x_boxes; ++i)
+              tma_load_2d_pair(xdst + i * kGrpXThinBytes, &tmXt, fb, kx, x_row + i * kGrpXThinRows);
+          } else {
+            for (int i = 0; i < x_boxes; ++i)
+              tma_load_2d_pair(xdst + i * kGrpXBoxBytes, &tmX, fb, kx, x_row + i * kGrpXBoxRows);
+          }
           if (++stage == kGrpStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -401,8 +424,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    uint8_t* stg = smStg + (warp - 4) * kGrpStgBytes;
-    const uint32_t stg_addr = smem_addr(stg);
+    const uint32_t stg_base = smem_addr(smStg + (warp - 4) * kGrpStgBufs * kGrpStgBytes);
+    int sbuf = 0;
+    bool last_tma = false;  // the previous chunk (other buffer) committed a TMA store
     int acc = 0;
     uint32_t acc_phase = 0;
     GrpWalker gw;
@@ -439,6 +463,20 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             if constexpr (EPI == 3) v[j] = grp_gelu(v[j]);
           }
         }
+        // A chunk of 32 tokens all inside the group and 32 features all
+        // inside N leaves through a TMA store of the transposed block; a
+        // chunk at the group's end (whose box would cover the next group's
+        // rows) or at the last features uses masked stores.
+        const bool whole = c0 + 32 <= tl.nt && n_base + 32 <= p.N;
+        const uint32_t stg_addr = stg_base + (uint32_t)(sbuf * kGrpStgBytes);
+        // Every TMA store that read this buffer has finished reading it: all
+        // but the newest committed store when that one used the other
+        // buffer, else all of them.
+        if (lane == 0) {
+          if (last_tma) bulk_wait_group_read<1>();
+          else bulk_wait_group_read<0>();
+        }
+        __syncwarp();
         // Transpose: lane (feature) writes column `lane` of the [token][feature] block.
         if constexpr (OUT_F32) {
 #pragma unroll
@@ -451,6 +489,17 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg_addr + j * 64u + lane * 2u),
                          "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
           }
+        }
+        if (whole) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, stg_addr, n_base, tl.t0 + c0);
+            bulk_commit_group();
+          }
+          sbuf ^= 1;
+          last_tma = true;
+          continue;
         }
         __syncwarp();
         // Row segments of C: 64 B (bf16) / 128 B (fp32) per token row.
@@ -487,12 +536,16 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           }
         }
         __syncwarp();
+        sbuf ^= 1;
+        last_tma = false;
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(acc), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_group<0>();  // this warp's TMA stores are complete
+    __syncwarp();
   }
 
   tc_fence_before_sync();

@@ -48,13 +48,12 @@
 //
 // Schedule: items are dealt round-robin to the persistent CTAs for as many
 // full waves as there are; the items of the last, partial wave (when it is
-// at most half full) are split by key blocks over ALL CTAs ("stream-K":
-// CTA c takes units [lo(c), lo(c+1)) of the remaining (item, key block)
-// units, lo(c) = U*c/G).  A CTA that covers an item's later key blocks
-// without its first publishes its un-normalised O, row maxima m and row sums
-// l in the workspace and releases a per-warp flag; the CTA holding the
-// item's first block (processed at the end of its range, after the others
-// published at the start of theirs) merges them with its own:
+// at most half full) are split by key blocks over ALL CTAs: each tail item
+// gets a contiguous group of 2 or more CTAs, which cut its key blocks into
+// equal contiguous shares (one fragment per CTA).  A CTA that covers an
+// item's later key blocks without its first publishes its un-normalised O,
+// row maxima m and row sums l in the workspace and releases a per-warp
+// flag; the CTA holding the item's first block merges them with its own:
 // m* = max m_i,  l* = sum l_i 2^(m_i - m*),  O = sum O_i 2^(m_i - m*) / l*.
 // Flags carry a per-call value from the host.  Waits go only from lower to
 // higher CTA indices and the launch is cooperative, so every waited-for CTA
@@ -84,8 +83,13 @@ constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 32 KB: two 64-wide 
 // v_empty[S], s_full[2], p_full[2], pv_done[2], o_empty, o_staged,
 // merge_full[4] (one per softmax warp)
 constexpr int kAttnNumBars = 3 + 4 * kAttnStages + 12;
+// Users whose candidate offsets are copied into shared memory at the start
+// (the item walkers then read them there instead of through dependent
+// global loads); calls with more users read them from global memory.
+constexpr int kAttnSmemUsers = 256;
+constexpr size_t kAttnOffsBytes = (kAttnSmemUsers + 1) * 4 + 12;  // padded to 16 bytes
 constexpr size_t kAttnSmemBytes = (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
-                                  512 /*barriers*/ + 1024 /*align*/;
+                                  512 /*barriers*/ + kAttnOffsBytes + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kAttnNumBars * 8 + 32 <= 512, "barrier area + TMEM slot, abort flag, item count");
 // TMEM columns: Q at 0 (64 columns of bf16 pairs), S/P buffers at 64 and
@@ -136,7 +140,7 @@ struct AttnArgs {
   WsHeader* ws;
   unsigned long long timeout_ns;
   uint32_t epoch;        // this call's flag value (split only; nonzero, distinct from earlier calls')
-  int split;             // 1: split the last partial wave by key blocks (stream-K)
+  int split;             // 1: split the last partial wave by key blocks
   uint32_t* flags;       // [kAttnMaxCtas][4]   (split only)
   float* slots;          // [kAttnMaxCtas][kAttnSlotFloats]
 };
@@ -228,11 +232,12 @@ struct AttnWalker {
   int u;
   long long base, count;
   int q0, nq, tiles;
+  const int* offs;  // the user offsets: a shared-memory copy, or p.uoff
 
   __device__ __forceinline__ void load(const AttnArgs& p) {
     if (u >= p.num_users) { count = 0; return; }
-    int a = __ldg(p.uoff + u);
-    int b = __ldg(p.uoff + u + 1);
+    int a = offs[u];
+    int b = offs[u + 1];
     a = min(max(a, 0), p.num_cand);
     b = min(max(b, a), p.num_cand);
     q0 = a * p.Lq;
@@ -240,7 +245,8 @@ struct AttnWalker {
     tiles = (nq + kAttnBM - 1) / kAttnBM;
     count = (long long)tiles * p.H;
   }
-  __device__ __forceinline__ void init(const AttnArgs& p) {
+  __device__ __forceinline__ void init(const AttnArgs& p, const int* offsets) {
+    offs = offsets;
     u = 0;
     base = 0;
     load(p);
@@ -272,11 +278,26 @@ struct AttnFrag {
 };
 
 // The schedule every role walks in the same order: whole items round-robin
-// (t = blockIdx.x, + gridDim.x, ... below n_full), then this CTA's share
-// [u, hi) of the remaining (item, key block) units.
+// (t = blockIdx.x, + gridDim.x, ... below n_full), then at most one tail
+// fragment.  The R tail items (the last, partial wave) are spread over all
+// CTAs: tail item r owns the contiguous CTAs [c0(r), c0(r+1)),
+// c0(r) = floor(r G / R) (2 or more CTAs each, since R <= G / 2), and the
+// k CTAs of an item split its key blocks evenly: the i-th takes blocks
+// [floor(i nblk / k), floor((i + 1) nblk / k)).  Every tail CTA has one
+// contiguous fragment of one item, so the tail costs one item boundary and
+// at most ceil(nblk / 2) blocks; the CTA holding the item's first block
+// merges the partials of the others, which all have higher indices.
 struct AttnSched {
-  long long n_full, t, u, hi, base, units;
+  long long n_full, t;
   int nblk;
+  long long tail_item;   // this CTA's tail item (-1: none)
+  int tail_jb, tail_je;  // its key blocks
+  int tail_i, tail_k;    // its rank among the item's CTAs, and their count
+  bool tail_left;
+
+  __device__ __forceinline__ static int part(int i, int k, int nb) {
+    return (int)((long long)i * nb / k);
+  }
 
   __device__ __forceinline__ void init(long long n_items, int nblk_, bool split) {
     nblk = nblk_;
@@ -286,14 +307,22 @@ struct AttnSched {
     const long long tail = n_items % G;
     n_full = split && 2 * tail <= G ? n_items - tail : n_items;
     t = blockIdx.x;
-    base = n_full * nblk;
-    units = (n_items - n_full) * nblk;
-    u = lo(blockIdx.x);
-    hi = lo(blockIdx.x + 1);
-  }
-  // first tail unit of CTA c
-  __device__ __forceinline__ long long lo(long long c) const {
-    return base + units * c / (long long)gridDim.x;
+    const long long R = n_items - n_full;
+    tail_item = -1;
+    tail_left = false;
+    if (R > 0) {
+      const long long c = blockIdx.x;
+      const long long r = ((c + 1) * R - 1) / G;
+      const long long c0 = r * G / R, c1 = (r + 1) * G / R;
+      tail_i = (int)(c - c0);
+      tail_k = (int)(c1 - c0);
+      tail_jb = part(tail_i, tail_k, nblk);
+      tail_je = part(tail_i + 1, tail_k, nblk);
+      if (tail_je > tail_jb) {
+        tail_item = n_full + r;
+        tail_left = true;
+      }
+    }
   }
   __device__ __forceinline__ bool next(AttnFrag& f) {
     if (t < n_full) {
@@ -303,11 +332,11 @@ struct AttnSched {
       t += gridDim.x;
       return true;
     }
-    if (u < hi) {
-      f.item = u / nblk;
-      f.jb = (int)(u - f.item * nblk);
-      f.je = (int)min((long long)nblk, hi - f.item * nblk);
-      u = f.item * nblk + f.je;
+    if (tail_left) {
+      f.item = tail_item;
+      f.jb = tail_jb;
+      f.je = tail_je;
+      tail_left = false;
       return true;
     }
     return false;
@@ -315,12 +344,15 @@ struct AttnSched {
 };
 
 // Items (user, head, 128-row query tile) of the whole call; offsets clamped
-// as the walker clamps them.  One warp.
-__device__ __forceinline__ long long attn_count_items(const AttnArgs& p, uint32_t lane) {
+// as the walker clamps them.  One warp; when `soffs` is given (at most
+// kAttnSmemUsers users) it also copies the offsets there.
+__device__ __forceinline__ long long attn_count_items(const AttnArgs& p, uint32_t lane, int* soffs) {
   long long cnt = 0;
+  if (soffs && lane == 0) soffs[p.num_users] = __ldg(p.uoff + p.num_users);
   for (int u = (int)lane; u < p.num_users; u += 32) {
     int a = __ldg(p.uoff + u);
     int b = __ldg(p.uoff + u + 1);
+    if (soffs) soffs[u] = a;
     a = min(max(a, 0), p.num_cand);
     b = min(max(b, a), p.num_cand);
     cnt += ((long long)(b - a) * p.Lq + kAttnBM - 1) / kAttnBM;
@@ -359,6 +391,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   long long* n_items_s = reinterpret_cast<long long*>(tmem_slot + 4);  // 8-byte aligned
+  int* soffs = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 512);
+  const int* offs = p.num_users <= kAttnSmemUsers ? soffs : p.uoff;
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
@@ -410,7 +444,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tmem_relinquish<1>();
   }
   if (warp == 3) {
-    const long long n = attn_count_items(p, lane);
+    const long long n = attn_count_items(p, lane, p.num_users <= kAttnSmemUsers ? soffs : nullptr);
     if (lane == 0) *n_items_s = n;
   }
   tc_fence_before_sync();
@@ -426,7 +460,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       AttnWalker w;
-      w.init(p);
+      w.init(p, offs);
       AttnSched sc;
       sc.init(n_items, nblk, p.split != 0);
       AttnFrag f;
@@ -570,7 +604,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       return true;
     };
     AttnWalker w;
-    w.init(p);
+    w.init(p, offs);
     AttnSched sc;
     sc.init(n_items, nblk, p.split != 0);
     AttnFrag f;
@@ -783,25 +817,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // shares copied into this warp's 48 KB of the rings, and the running
         // (m, l, O) rescaled in TMEM:  m' = max(m, m_k),
         // l' = l 2^(m - m') + sum l_k 2^(m_k - m'),  O' likewise.
-        const long long item_end = (f.item + 1) * nblk;
         const uint32_t stg = smem_addr(sK) + (uint32_t)(q * kAttnMergeBatch * kAttnWarpPartBytes);
-        // Walk the CTAs after this one: lo(c) = base + floor(units * c / G)
-        // stepped by the quotient and remainder of units / G (no 64-bit
-        // division per CTA), skipping CTAs whose range is empty.
-        const long long G = gridDim.x;
-        const long long dq = sc.units / G, dr = sc.units % G;
-        long long c2 = (long long)blockIdx.x + 1;
-        long long lo_c = sc.lo(c2), rem = (sc.units * c2) % G;
+        // The item's CTAs after this one (ranks tail_i + 1 .. tail_k - 1,
+        // at blockIdx.x + 1, ...), skipping those whose share of the key
+        // blocks is empty.
+        int pi = sc.tail_i + 1;
         auto next_partial = [&]() -> int {
-          while (c2 < G && lo_c < item_end) {
-            const bool wrap = rem + dr >= G;
-            const long long lo_n = lo_c + dq + (wrap ? 1 : 0);
-            const int c = (int)c2;
-            const bool nonempty = lo_n > lo_c;
-            lo_c = lo_n;
-            rem = wrap ? rem + dr - G : rem + dr;
-            ++c2;
-            if (nonempty) return c;
+          while (pi < sc.tail_k) {
+            const int i = pi++;
+            if (AttnSched::part(i + 1, sc.tail_k, nblk) > AttnSched::part(i, sc.tail_k, nblk))
+              return (int)blockIdx.x + (i - sc.tail_i);
           }
           return -1;
         };
