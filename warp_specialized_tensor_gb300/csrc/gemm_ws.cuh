@@ -129,6 +129,32 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[32], const __nv_bfloat
   }
 }
 
+// Packed fp32 pairs (one 64-bit register: low half = first element), for the
+// row statistics: half the instructions of the scalar form, each lane rounded
+// as its scalar operation.
+__device__ __forceinline__ uint64_t f2_bf16x2(uint32_t w) {  // bf16 pair -> fp32 pair (exact)
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_splat(float x) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t a) { return __uint_as_float((uint32_t)a); }
+__device__ __forceinline__ float f2_hi(uint64_t a) { return __uint_as_float((uint32_t)(a >> 32)); }
+
 // Row normalisation of 32 accumulator columns [col, col+32) of one row:
 // RMSNorm v *= r; LayerNorm v = r*v - (r*mu)*s[n] (s the column sums of B, the
 // same for every row: the warp's lanes read the same addresses).  The sums
@@ -383,7 +409,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       // Statistician 37(3), 1983): var = E[d^2] - E[d]^2 cancels only as
       // much as (c - mu)^2 / var, which is small because c is a value of the
       // row, where the unshifted E[a^2] - mu^2 cancels mu^2 / var.
-      float ss = 0.0f, sm = 0.0f, c = 0.0f;
+      // The sums are kept as packed pairs (even and odd K positions); the
+      // halves are added at the end.
+      uint64_t ss2 = 0, sm2 = 0;
+      float c = 0.0f;
+      uint64_t negc2 = 0;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         // the MMAs that read this stage completed (their commit, multicast
         // to both CTAs of a pair, arrives on consumed[s])
@@ -404,7 +434,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             // 16-byte chunk 0, stored at chunk (0 ^ (r & 7)) by the swizzle
             uint32_t w;
             asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(row_addr + ((uint32_t)(r & 7) << 4)));
-            c = __bfloat162float(__ushort_as_bfloat16((unsigned short)(w & 0xffffu)));
+            c = __uint_as_float(w << 16);
+            negc2 = f2_splat(-c);
           }
         }
         // K positions past K in the last block are zero-filled by the copy;
@@ -420,19 +451,18 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             const uint32_t w[4] = {w0, w1, w2, w3};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+              const uint64_t f2 = f2_bf16x2(w[e]);
               if constexpr (NORM == 1) {
-                ss = fmaf(f.x, f.x, ss);
-                ss = fmaf(f.y, f.y, ss);
+                ss2 = f2_fma(f2, f2, ss2);
               } else {
-                float dx = f.x - c, dy = f.y - c;
+                uint64_t d2 = f2_add(f2, negc2);
                 if constexpr (decltype(masked)::value) {
-                  if (8 * j + 2 * e >= kvalid) dx = 0.0f;
-                  if (8 * j + 2 * e + 1 >= kvalid) dy = 0.0f;
+                  const float dx = 8 * j + 2 * e < kvalid ? f2_lo(d2) : 0.0f;
+                  const float dy = 8 * j + 2 * e + 1 < kvalid ? f2_hi(d2) : 0.0f;
+                  asm("mov.b64 %0, {%1, %2};" : "=l"(d2) : "f"(dx), "f"(dy));
                 }
-                ss = fmaf(dx, dx, ss);
-                ss = fmaf(dy, dy, ss);
-                sm += dx + dy;
+                ss2 = f2_fma(d2, d2, ss2);
+                sm2 = f2_add(sm2, d2);
               }
             }
           }
@@ -445,9 +475,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       }
       if (!ok) break;
       if (!warp_wait_phase(guard, scle_bar(acc), acc_phase ^ 1u, (kRoleEpilogue << 16) | 0x500 | acc)) break;
+      const float ss = f2_lo(ss2) + f2_hi(ss2);
       if constexpr (NORM == 1) {
         row_scale[acc * kBM + r] = rsqrtf(ss * p.inv_k + p.eps);
       } else {
+        const float sm = f2_lo(sm2) + f2_hi(sm2);
         // LayerNorm: mean = c + E[d], biased variance = E[d^2] - E[d]^2
         // (fp32, clamped at 0)
         const float dm = sm * p.inv_k;

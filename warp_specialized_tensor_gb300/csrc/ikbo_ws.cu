@@ -29,8 +29,17 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
     set_error("ikbo: W tile of %zu bytes leaves too little shared memory for the ring", w_bytes);
     return ST_UNSUPPORTED;
   }
+  // Ring depth: 4 stages of 16 KB.  With one CTA per SM, 4 x 16 KB in
+  // flight per SM already covers HBM's bandwidth-latency product (about
+  // 6.8 MB at 6.8 TB/s and ~1 us, against 152 x 64 KB); a deeper ring only
+  // lengthens every request's queue, including the user partials' stores,
+  // their release fences and the candidates' flag polls, which gate each
+  // CTA's first epilogue.  Measured on GB300 (64 users x 128 candidates,
+  // one box, interleaved): 3 or 4 stages 0.0546 ms, 6 stages 0.0575 ms,
+  // 12 stages (shared memory permitting) 0.0598 ms.
+  constexpr int kIkboRingStages = 4;
   int stages = (int)((smem_cap - fixed) / kIkboABytes);
-  if (stages > kIkboMaxStages) stages = kIkboMaxStages;
+  if (stages > kIkboRingStages) stages = kIkboRingStages;
   a.stages = stages;
   a.slots = 512 / pr.O < kIkboMaxSlots ? 512 / pr.O : kIkboMaxSlots;
   a.uoff = pr.uoff;

@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   uint8_t* smA = smW + align_up((size_t)kb_w * w_kb_bytes, 1024);
   uint8_t* smY = smA + (size_t)p.stages * kIkboABytes;  // output staging (kIkboStgTotal bytes)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smY + kIkboStgTotal);
-  // bars: full[stages] | empty[stages] | accf[slots] | acce[slots] | w
-  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
+  // bars: full[stages] | empty[stages] | accf[slots] | acce[slots] | w | users_done
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * kIkboMaxStages + 2 * kIkboMaxSlots + 2);
   uint32_t* tmem_slot = misc;                       // [0]
   volatile uint32_t* abort_flag = misc + 1;         // [1]
   uint32_t* cnt = misc + 4;                         // [4 .. 4+slots): user-publish counters
@@ -103,6 +103,16 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   auto accf_bar = [&](int a) { return bar_base + 8u * (2 * kIkboMaxStages + a); };
   auto acce_bar = [&](int a) { return bar_base + 8u * (2 * kIkboMaxStages + kIkboMaxSlots + a); };
   const uint32_t w_bar = bar_base + 8u * (2 * kIkboMaxStages + 2 * kIkboMaxSlots);
+  // users_done: this CTA's user partials are all published (see the producer)
+  const uint32_t ud_bar = bar_base + 8u * (2 * kIkboMaxStages + 2 * kIkboMaxSlots + 1);
+  const int kb_w0 = p.kb_u + p.kb_c;
+  const int n_user_items0 =
+      blockIdx.x < (unsigned)p.num_users ? (p.num_users - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // K-blocks of the first item loaded by thread 0 before the CTA-wide
+  // barrier (they need only the barriers it has just initialised)
+  const int first_nkb = n_user_items0 > 0 ? p.kb_u
+                        : (p.split[blockIdx.x] < p.split[blockIdx.x + 1] ? p.kb_c : 0);
+  const int pre_kb = first_nkb < p.stages ? first_nkb : p.stages;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -115,11 +125,28 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
       cnt[a] = 0;
     }
     mbar_init(w_bar, 1);
+    mbar_init(ud_bar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
+    // Start W^T and the first item's K-blocks now rather than after the
+    // CTA-wide barrier and the tensor-memory allocation.
+    mbar_arrive_expect_tx(w_bar, (uint32_t)(kb_w0 * p.O * 128));
+    for (int j = 0; j < kb_w0; ++j) {
+      const int x = j < p.kb_u ? j * 64 : p.Du + (j - p.kb_u) * 64;
+      tma_load_2d(smem_addr(smW + j * p.O * 128), &tmW, w_bar, x, 0);
+    }
+    {
+      const bool user0 = n_user_items0 > 0;
+      const int idx0 = user0 ? (int)blockIdx.x : p.split[blockIdx.x];
+      for (int kb = 0; kb < pre_kb; ++kb) {
+        mbar_arrive_expect_tx(full_bar(kb), kIkboABytes);
+        const uint32_t dA = smem_addr(smA + kb * kIkboABytes);
+        tma_load_3d(dA, user0 ? &tmU : &tmC, full_bar(kb), 0, kb * 64, idx0);
+        tma_load_3d(dA + kIkboABytes / 2, user0 ? &tmU : &tmC, full_bar(kb), 64, kb * 64, idx0);
+      }
+    }
     tma_prefetch_desc(&tmU);
     tma_prefetch_desc(&tmC);
-    tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmY);
   }
   if (warp == 2) {
@@ -141,21 +168,25 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      // W^T, resident for the whole kernel.
-      mbar_arrive_expect_tx(w_bar, (uint32_t)(kb_w * w_kb_bytes));
-      for (int j = 0; j < kb_w; ++j) {
-        const int x = j < p.kb_u ? j * 64 : p.Du + (j - p.kb_u) * 64;
-        tma_load_2d(smem_addr(smW + j * w_kb_bytes), &tmW, w_bar, x, 0);
-      }
-      int stage = 0;
-      uint32_t phase = 0;
+      // W^T (resident for the whole kernel) and the first item's first
+      // K-blocks were issued before the CTA-wide barrier.
+      int stage = pre_kb == p.stages ? 0 : pre_kb;
+      uint32_t phase = pre_kb == p.stages ? 1u : 0u;
       bool ok = true;
       for (int it = 0; it < n_items && ok; ++it) {
         const bool is_user = it < n_user_items;
         const int idx = is_user ? (int)blockIdx.x + it * (int)gridDim.x : c_lo + (it - n_user_items);
         const int nkb = is_user ? p.kb_u : p.kb_c;
         const CUtensorMap* m = is_user ? &tmU : &tmC;
-        for (int kb = 0; kb < nkb; ++kb) {
+        if (it == n_user_items && n_user_items > 0) {
+          // Hold this CTA's candidate loads until its user partials are
+          // published.  The publishing warps' GPU-scope fences wait for the
+          // SM's outstanding memory traffic; with a ring of candidate loads
+          // in flight behind them they took ~10 us (measured on GB300),
+          // and every CTA's candidates wait for some user's partial.
+          if (!wait_phase(guard, ud_bar, 0, (kRoleProducer << 16) | 0x300)) break;
+        }
+        for (int kb = (it == 0 ? pre_kb : 0); kb < nkb; ++kb) {
           if (!wait_phase(guard, empty_bar(stage), phase ^ 1u, (kRoleProducer << 16) | stage)) {
             ok = false;
             break;
@@ -284,6 +315,7 @@ __global__ void __launch_bounds__(kIkboThreads, 1)
           if ((old & 3u) == 3u) {
             fence_acq_rel_gpu();
             st_release_gpu(p.flags + idx, target);
+            if (it == n_user_items - 1) mbar_arrive(ud_bar);
           }
         }
       } else {
