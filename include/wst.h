@@ -54,8 +54,9 @@
  *    workspace must not be used by two calls that can run at the same time.
  *  - Errors found on the host are returned before anything is enqueued.
  *    Errors found on the device (a bounded wait that ran out, inconsistent
- *    device offsets) are latched in the workspace; wst_sync_status reads and
- *    clears them.  No call aborts, traps or throws.
+ *    device offsets, a row index out of range in wst_permute_rows) are
+ *    latched in the workspace; wst_sync_status reads and clears them.  No
+ *    call aborts, traps or throws.
  */
 #ifndef WST_H_
 #define WST_H_
@@ -219,6 +220,69 @@ wst_status wst_grouped_gemm_bf16(int G, int M_total, int N, int K,
                                  const void* bias, long strideBias,
                                  void* C, long ldc, wst_dtype c_type,
                                  wst_epilogue epi, void* workspace, void* stream);
+
+/*
+ * Expert parallelism: the grouped GEMM's experts spread over the R ranks
+ * (GPUs) of a node ("How We Built TLX: A Hardware-Native GPU Compiler for
+ * Production ML at Scale", "Case Study 3: Distributed Grouped GEMM for LLM
+ * Pretraining" and "TLX in Production": the distributed grouped GEMM of
+ * mixture-of-experts pretraining).  G experts, G divisible by R; rank r owns
+ * experts [r*G/R, (r+1)*G/R).  A token t routed to k experts forms the pairs
+ * p = t*k + s (s < k).  One layer on a rank:
+ *   1. wst_ep_dispatch_plan on the rank's routing table (host);
+ *   2. exchange the per-(rank, local expert) counts (an all-to-all);
+ *   3. wst_permute_rows gathers the token rows of the pairs in send order;
+ *   4. all-to-all of the rows (send_counts out, the received counts in);
+ *   5. wst_ep_receive_plan orders the received rows by local expert;
+ *      wst_permute_rows gathers them, wst_grouped_gemm_bf16 multiplies them
+ *      by the rank's experts (group offsets from the plan);
+ *   6. wst_permute_rows scatters the products back to received order, the
+ *      reverse all-to-all returns them, and wst_permute_rows scatters them
+ *      to their pairs.
+ * The exchanges are the caller's collectives (for example NCCL); the plans
+ * are host functions and need no GPU.
+ *
+ * wst_ep_dispatch_plan: HOST arrays.
+ *   routing            int32 [num_tokens][top_k], expert ids in [0, num_experts)
+ *   send_counts        out int32 [world_size]: pairs sent to each rank
+ *   send_group_counts  out int32 [num_experts]: pairs per expert (entry
+ *                      r*G/R + j: rank r's local expert j)
+ *   send_pairs         out int32 [num_tokens*top_k]: the pair carried by each
+ *                      send row, ordered by destination rank, then local
+ *                      expert, then pair id
+ * Returns WST_ERR_INVALID_ARG for a bad size, an expert id out of range or
+ * num_experts not divisible by world_size.
+ */
+wst_status wst_ep_dispatch_plan(int num_tokens, int top_k, const int* routing, int num_experts,
+                                int world_size, int* send_counts, int* send_group_counts,
+                                int* send_pairs);
+
+/*
+ * wst_ep_receive_plan: HOST arrays.  Rows arrive from the world_size ranks
+ * in source order, each source's block ordered by local expert, with
+ * recv_group_counts[s][e] rows from source s for local expert e.
+ *   group_offsets  out int32 [experts_per_rank+1]: the grouped GEMM's offsets
+ *                  of the expert-major order
+ *   expert_rows    out int32 [total received rows]: expert-major row i is
+ *                  received row expert_rows[i] (local expert e, then source s)
+ */
+wst_status wst_ep_receive_plan(int world_size, int experts_per_rank, const int* recv_group_counts,
+                               int* group_offsets, int* expert_rows);
+
+/*
+ * Row permutation on the GPU: for i < n_rows,
+ *   dst row (d_dst_index ? d_dst_index[i] : i) = src row (d_src_index ? d_src_index[i] : i).
+ * src, dst: DEVICE pointers, rows of row_bytes bytes at src_stride /
+ * dst_stride bytes apart (row_bytes and strides multiples of 16, pointers
+ * 16-byte aligned); the index arrays are DEVICE int32 (or NULL), and the
+ * source / destination hold n_src_rows / n_dst_rows rows.  An index outside
+ * them skips the row and latches WST_ERR_INVALID_ARG in `workspace` (a
+ * zero-filled workspace of at least wst_workspace_size(0, 0, 0) bytes) for
+ * wst_sync_status.  Asynchronous on `stream`.
+ */
+wst_status wst_permute_rows(int n_rows, size_t row_bytes, const void* src, size_t src_stride,
+                            const int* d_src_index, int n_src_rows, void* dst, size_t dst_stride,
+                            const int* d_dst_index, int n_dst_rows, void* workspace, void* stream);
 
 /*
  * IKBO linear compression.  Candidates of user u are [off[u], off[u+1]) of

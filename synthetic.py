@@ -86,6 +86,25 @@ def top2_routing(tokens: int, experts: int, g: torch.Generator, k: int = 2):
     return token_of[order], offsets
 
 
+def routing_table(tokens: int, experts: int, k: int, g: torch.Generator) -> torch.Tensor:
+    """int32 [tokens, k]: each token's k DISTINCT experts, uniformly at random."""
+    if k > experts:
+        raise ValueError("k > experts")
+    return torch.rand(tokens, experts, generator=g).argsort(dim=1)[:, :k].to(torch.int32).contiguous()
+
+
+def moe_tokens(tokens: int, experts: int, K: int, N: int, topk: int = 2, std: float = 0.02,
+               seed: int = SEED_BASE + 6):
+    """Token-major MoE layer inputs (for the expert-parallel layout): X
+    [tokens, K] bf16, routing int32 [tokens, topk] (distinct experts per
+    token), B [experts, N, K] bf16 (K contiguous)."""
+    g = _gen(seed)
+    X = _normal(g, (tokens, K), std)
+    routing = routing_table(tokens, experts, topk, g)
+    B = _normal(g, (experts, N, K), std)
+    return {"X": X, "routing": routing, "B": B}
+
+
 def grouped(experts: int = 64, tokens: int = 16384, K: int = 4096, N: int = 1536,
             topk: int = 2, std: float = 0.02, seed: int = SEED_BASE + 2,
             group_sizes=None):

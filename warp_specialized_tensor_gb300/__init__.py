@@ -27,7 +27,7 @@ __all__ = [
     "wst_ikbo_attention_workspace_size", "attention_workspace",
     "wst_sync_status", "wst_status_string", "wst_set_option", "wst_get_option", "option",
     "OPT_GROUPED_SCHEDULE", "OPT_DENSE_CTA_GROUP", "SCHED_STATIC", "SCHED_CLC",
-    "wst_version",
+    "wst_version", "wst_ep_dispatch_plan", "wst_ep_receive_plan", "wst_permute_rows",
 ]
 
 # enums of include/wst.h
@@ -92,6 +92,13 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_ikbo_attention_bf16.restype = I
         lib.wst_ikbo_attention_workspace_size.argtypes = []
         lib.wst_ikbo_attention_workspace_size.restype = Z
+        IP = ctypes.POINTER(ctypes.c_int)
+        lib.wst_ep_dispatch_plan.argtypes = [I, I, IP, I, I, IP, IP, IP]
+        lib.wst_ep_dispatch_plan.restype = I
+        lib.wst_ep_receive_plan.argtypes = [I, I, IP, IP, IP]
+        lib.wst_ep_receive_plan.restype = I
+        lib.wst_permute_rows.argtypes = [I, Z, P, Z, P, I, P, Z, P, I, P, P]
+        lib.wst_permute_rows.restype = I
         lib.wst_set_option.argtypes = [I, I]
         lib.wst_set_option.restype = I
         lib.wst_get_option.argtypes = [I, ctypes.POINTER(ctypes.c_int)]
@@ -453,3 +460,74 @@ def wst_ikbo_linear_compress_noalloc(U, Cf, W, user_offsets, Y, status=None,
 def wst_sync_status(workspace, stream=None) -> int:
     """Synchronize the stream; return (and clear) the first device-side error code."""
     return int(load_library().wst_sync_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+# ----------------------------------------------------------------------------
+# expert parallelism: host plans and GPU row movement
+# ----------------------------------------------------------------------------
+def _i32p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def wst_ep_dispatch_plan(routing, num_experts: int, world_size: int):
+    """Host plan of the pairs this rank sends (see include/wst.h).
+
+    routing: int32 array [tokens, top_k] of expert ids (numpy or CPU tensor).
+    Returns numpy int32 arrays (send_counts [world_size], send_group_counts
+    [num_experts], send_pairs [tokens*top_k])."""
+    import numpy as np
+    r = np.ascontiguousarray(np.asarray(routing, dtype=np.int32))
+    if r.ndim != 2:
+        raise ValueError("routing must be [tokens, top_k]")
+    T, k = r.shape
+    send_counts = np.zeros(world_size, dtype=np.int32)
+    group_counts = np.zeros(num_experts, dtype=np.int32)
+    pairs = np.zeros(max(T * k, 1), dtype=np.int32)
+    _check(load_library().wst_ep_dispatch_plan(T, k, _i32p(r), num_experts, world_size,
+                                               _i32p(send_counts), _i32p(group_counts), _i32p(pairs)),
+           "wst_ep_dispatch_plan")
+    return send_counts, group_counts, pairs[:T * k]
+
+
+def wst_ep_receive_plan(recv_group_counts):
+    """Host plan ordering received rows by local expert.
+
+    recv_group_counts: int32 [world_size, experts_per_rank].  Returns numpy
+    int32 arrays (group_offsets [experts_per_rank+1], expert_rows [rows])."""
+    import numpy as np
+    c = np.ascontiguousarray(np.asarray(recv_group_counts, dtype=np.int32))
+    if c.ndim != 2:
+        raise ValueError("recv_group_counts must be [world_size, experts_per_rank]")
+    R, E = c.shape
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    rows = np.zeros(max(int(c.astype(np.int64).sum()), 1), dtype=np.int32)
+    _check(load_library().wst_ep_receive_plan(R, E, _i32p(c), _i32p(offsets), _i32p(rows)),
+           "wst_ep_receive_plan")
+    return offsets, rows[:int(offsets[-1])]
+
+
+def wst_permute_rows(src, dst, src_index=None, dst_index=None, n_rows=None, workspace=None,
+                     stream=None) -> None:
+    """dst[dst_index[i] (or i)] = src[src_index[i] (or i)] for i < n_rows, on the GPU.
+
+    src, dst: CUDA tensors of rows (2-D, last dimension contiguous, the same
+    bytes per row); src_index / dst_index: CUDA int32 tensors or None;
+    n_rows defaults to the index length (else the source's rows)."""
+    for t, n in ((src, "src"), (dst, "dst")):
+        _need(t, n, None, (2,))
+    row_bytes = src.shape[1] * src.element_size()
+    if dst.shape[1] * dst.element_size() != row_bytes:
+        raise ValueError("src and dst rows differ in size")
+    for t, n in ((src_index, "src_index"), (dst_index, "dst_index")):
+        if t is not None:
+            _need(t, n, torch.int32, (1,))
+    if n_rows is None:
+        idx = src_index if src_index is not None else dst_index
+        n_rows = idx.numel() if idx is not None else src.shape[0]
+    if workspace is None:
+        raise ValueError("workspace is required (see workspace())")
+    st = load_library().wst_permute_rows(
+        int(n_rows), row_bytes, src.data_ptr(), src.stride(0) * src.element_size(), _ptr(src_index),
+        src.shape[0], dst.data_ptr(), dst.stride(0) * dst.element_size(), _ptr(dst_index),
+        dst.shape[0], workspace.data_ptr(), _stream_handle(stream))
+    _check(st, "wst_permute_rows")

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwst.so")
 
-SOURCES = ["gemm_dense.cu", "grouped_ws.cu", "ikbo_ws.cu", "ikbo_attn.cu", "wst_api.cu"]
+SOURCES = ["gemm_dense.cu", "grouped_ws.cu", "ikbo_ws.cu", "ikbo_attn.cu", "wst_api.cu", "expert_parallel.cu"]
 HEADERS = ["sm103.cuh", "wst_common.cuh", "gemm_ws.cuh", "grouped_ws.cuh", "ikbo_ws.cuh", "ikbo_attn_ws.cuh",
            "wst_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

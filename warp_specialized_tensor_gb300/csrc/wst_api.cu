@@ -598,7 +598,8 @@ wst_status wst_sync_status(void* workspace, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return (wst_status)cuda_fail(e, "clearing the workspace error word");
   set_error("device error %u (info 0x%08x)", hdr[0], hdr[1]);
-  if (hdr[0] == WST_ERR_TIMEOUT || hdr[0] == WST_ERR_BAD_OFFSETS) return (wst_status)hdr[0];
+  if (hdr[0] == WST_ERR_TIMEOUT || hdr[0] == WST_ERR_BAD_OFFSETS || hdr[0] == WST_ERR_INVALID_ARG)
+    return (wst_status)hdr[0];
   return WST_ERR_CUDA;
 }
 
