@@ -103,11 +103,21 @@ typedef enum {
  *                             pairs on 256-row tiles when M > 128, else one
  *                             CTA per 128-row tile), 1 always one CTA per
  *                             128-row tile, 2 always CTA pairs.
+ *   WST_OPT_IKBO_SCHEDULE     candidate schedule of the IKBO linear
+ *                             compression (both entry points):
+ *                             WST_SCHED_STATIC (default: a persistent grid,
+ *                             each CTA's user items, then one contiguous
+ *                             candidate range balanced on the host) or
+ *                             WST_SCHED_CLC (one CTA per user item and per
+ *                             16-candidate chunk launched; running CTAs take
+ *                             over unstarted ones by hardware cluster launch
+ *                             control).
  * wst_set_option returns WST_ERR_INVALID_ARG for an unknown option or value.
  */
 typedef enum {
   WST_OPT_GROUPED_SCHEDULE = 0,
-  WST_OPT_DENSE_CTA_GROUP = 1
+  WST_OPT_DENSE_CTA_GROUP = 1,
+  WST_OPT_IKBO_SCHEDULE = 2
 } wst_option;
 
 typedef enum { WST_SCHED_STATIC = 0, WST_SCHED_CLC = 1 } wst_schedule;

@@ -1,5 +1,5 @@
 """GPU parity: IKBO linear compression (in-kernel user broadcast) vs the
-materialised-broadcast fp64 oracle."""
+materialised-broadcast fp64 oracle, under both candidate schedules."""
 import numpy as np
 import pytest
 import torch
@@ -16,6 +16,15 @@ def wst():
     import warp_specialized_tensor_gb300 as w
     w.load_library()
     return w
+
+
+@pytest.fixture(autouse=True, params=["static", "clc"])
+def sched(request, wst):
+    # Every test under both candidate schedules: the static persistent split
+    # and hardware cluster launch control (WST_OPT_IKBO_SCHEDULE).
+    value = wst.SCHED_CLC if request.param == "clc" else wst.SCHED_STATIC
+    with wst.option(wst.OPT_IKBO_SCHEDULE, value):
+        yield request.param
 
 
 def run_ikbo(wst, d, ws=None):

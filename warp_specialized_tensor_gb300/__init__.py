@@ -26,7 +26,7 @@ __all__ = [
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
     "wst_ikbo_attention_workspace_size", "attention_workspace",
     "wst_sync_status", "wst_status_string", "wst_set_option", "wst_get_option", "option",
-    "OPT_GROUPED_SCHEDULE", "OPT_DENSE_CTA_GROUP", "SCHED_STATIC", "SCHED_CLC",
+    "OPT_GROUPED_SCHEDULE", "OPT_DENSE_CTA_GROUP", "OPT_IKBO_SCHEDULE", "SCHED_STATIC", "SCHED_CLC",
     "wst_version", "wst_ep_dispatch_plan", "wst_ep_receive_plan", "wst_permute_rows",
 ]
 
@@ -35,7 +35,7 @@ WST_OK, WST_ERR_INVALID_ARG, WST_ERR_ALIGNMENT, WST_ERR_UNSUPPORTED = 0, 1, 2, 3
 WST_ERR_CUDA, WST_ERR_TIMEOUT, WST_ERR_BAD_OFFSETS = 4, 5, 6
 F32, BF16 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_BIAS_SILU, EPI_BIAS_GELU = 0, 1, 2, 3
-OPT_GROUPED_SCHEDULE, OPT_DENSE_CTA_GROUP = 0, 1
+OPT_GROUPED_SCHEDULE, OPT_DENSE_CTA_GROUP, OPT_IKBO_SCHEDULE = 0, 1, 2
 SCHED_STATIC, SCHED_CLC = 0, 1
 _EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_silu": EPI_BIAS_SILU,
               "bias_gelu": EPI_BIAS_GELU}
@@ -168,8 +168,9 @@ def _need(t, name, dtype=None, dims=None):
 # process-wide options
 # ----------------------------------------------------------------------------
 def wst_set_option(opt: int, value: int) -> None:
-    """Set a process-wide tuning option (OPT_GROUPED_SCHEDULE: SCHED_STATIC or
-    SCHED_CLC; OPT_DENSE_CTA_GROUP: 0 automatic, 1 single-CTA tiles, 2 pairs)."""
+    """Set a process-wide tuning option (OPT_GROUPED_SCHEDULE and
+    OPT_IKBO_SCHEDULE: SCHED_STATIC or SCHED_CLC; OPT_DENSE_CTA_GROUP: 0
+    automatic, 1 single-CTA tiles, 2 pairs)."""
     _check(load_library().wst_set_option(int(opt), int(value)), "wst_set_option")
 
 

@@ -90,8 +90,11 @@ __device__ __forceinline__ Tile dense_tile(const GemmArgs& p, long long t) {
 __device__ __forceinline__ float gelu_f(float x) { return x * normcdff(x); }
 
 __device__ __forceinline__ float silu_f(float x) {
-  // x * sigmoid(x); __expf overflows to +inf for very negative x, giving -0.
-  return __fdividef(x, 1.0f + __expf(-x));
+  // x * sigmoid(x), sigmoid(x) = (1 + tanh(x / 2)) / 2: one special-function
+  // instruction (tanh.approx) instead of two (exponential and reciprocal).
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return x * fmaf(0.5f, t, 0.5f);
 }
 
 template <int EPI>

@@ -184,7 +184,12 @@ static __device__ __noinline__ void grouped_check_offsets(const GroupedArgs& p) 
   if (bad) latch_error(p.ws, kErrBadOffsets, 2);
 }
 
-__device__ __forceinline__ float grp_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// x * sigmoid(x) with sigmoid(x) = (1 + tanh(x / 2)) / 2 (one tanh.approx).
+__device__ __forceinline__ float grp_silu(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return x * fmaf(0.5f, t, 0.5f);
+}
 // GELU(x) = x * Phi(x) (exact erf form, the CUDA math library's normcdff).
 __device__ __forceinline__ float grp_gelu(float x) { return x * normcdff(x); }
 

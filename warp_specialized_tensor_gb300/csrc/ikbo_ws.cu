@@ -88,8 +88,27 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   }
 
   const size_t smem = fixed + (size_t)stages * kIkboABytes;
-  if ((st = ensure_smem_attr((const void*)k_ikbo_ws, smem))) return st;
   cudaError_t e;
+  if (option_value(OPT_IKBO_SCHEDULE) == 1) {
+    // Cluster launch control: one CTA per unit (each user item, then chunks
+    // of kIkboClcChunk candidates); running CTAs take over unstarted ones.
+    a.chunk = kIkboClcChunk;
+    const long long units = (long long)pr.num_users + ((long long)pr.num_cand + kIkboClcChunk - 1) / kIkboClcChunk;
+    if (units > 0x7fffffffLL) {
+      set_error("ikbo: %lld units exceed the grid limit", units);
+      return ST_UNSUPPORTED;
+    }
+    if ((st = ensure_smem_attr((const void*)k_ikbo_ws<true>, smem))) return st;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)units, 1, 1);
+    cfg.blockDim = dim3(kIkboThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    e = cudaLaunchKernelEx(&cfg, k_ikbo_ws<true>, tmU, tmC, tmW, tmY, a);
+    if (e != cudaSuccess) return cuda_fail(e, "launch k_ikbo_ws (cluster launch control)");
+    return ST_OK;
+  }
+  if ((st = ensure_smem_attr((const void*)k_ikbo_ws<false>, smem))) return st;
   int grid = dev.num_sms < kIkboMaxGrid ? dev.num_sms : kIkboMaxGrid;
   const long long items = (long long)pr.num_users + pr.num_cand;
   if (items < grid) grid = (int)items;
@@ -127,7 +146,7 @@ int run_ikbo(const IkboProblem& pr, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_ikbo_ws, tmU, tmC, tmW, tmY, a);
+  e = cudaLaunchKernelEx(&cfg, k_ikbo_ws<false>, tmU, tmC, tmW, tmY, a);
   if (e != cudaSuccess) return cuda_fail(e, "launch k_ikbo_ws");
   return ST_OK;
 }

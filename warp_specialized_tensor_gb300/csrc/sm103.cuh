@@ -130,6 +130,15 @@ __device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) 
       : "memory");
 }
 
+// The same for a grid without clusters: the response lands in this CTA only.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          resp),
+      "r"(bar)
+      : "memory");
+}
+
 // Decodes a response: true, with the x index of the cancelled cluster's
 // first CTA, if a cluster was cancelled; false once none is left.
 __device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& first_x) {

@@ -622,6 +622,7 @@ wst_status wst_set_option(wst_option opt, int value) {
   switch ((int)opt) {
     case OPT_GROUPED_SCHEDULE: hi = 1; break;
     case OPT_DENSE_CTA_GROUP: hi = 2; break;
+    case OPT_IKBO_SCHEDULE: hi = 1; break;
     default: return fail(WST_ERR_INVALID_ARG, "unknown option %d", (int)opt);
   }
   if (value < 0 || value > hi)

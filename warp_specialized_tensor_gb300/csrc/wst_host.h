@@ -33,7 +33,7 @@ struct DeviceInfo {
 int current_device_info(DeviceInfo* out);  // Status
 
 // Process-wide tuning options (wst_option in include/wst.h).
-enum Option : int { OPT_GROUPED_SCHEDULE = 0, OPT_DENSE_CTA_GROUP = 1, OPT_COUNT = 2 };
+enum Option : int { OPT_GROUPED_SCHEDULE = 0, OPT_DENSE_CTA_GROUP = 1, OPT_IKBO_SCHEDULE = 2, OPT_COUNT = 3 };
 int option_value(int opt);
 
 unsigned long long wait_timeout_ns();
