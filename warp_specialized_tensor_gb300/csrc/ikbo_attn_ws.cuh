@@ -251,7 +251,11 @@ struct AttnWalker {
     base = 0;
     load(p);
   }
+  // Walk forward to the user holding item t (from the start again if t lies
+  // before the current user: a CTA's tail fragment, which can come first,
+  // has a higher item index than its whole items).
   __device__ __forceinline__ bool seek(const AttnArgs& p, long long t) {
+    if (t < base) init(p, offs);
     while (u < p.num_users && t >= base + count) {
       base += count;
       ++u;
@@ -286,7 +290,9 @@ struct AttnFrag {
 // [floor(i nblk / k), floor((i + 1) nblk / k)).  Every tail CTA has one
 // contiguous fragment of one item, so the tail costs one item boundary and
 // at most ceil(nblk / 2) blocks; the CTA holding the item's first block
-// merges the partials of the others, which all have higher indices.
+// merges the partials of the others, which all have higher indices.  CTAs
+// whose fragment starts past the item's first block run it before their
+// whole items (see next()).
 struct AttnSched {
   long long n_full, t;
   int nblk;
@@ -325,6 +331,19 @@ struct AttnSched {
     }
   }
   __device__ __forceinline__ bool next(AttnFrag& f) {
+    // A CTA that publishes a partial (its share starts past the item's first
+    // block) runs its tail fragment FIRST: its partial is then ready long
+    // before the merging CTA (which runs its fragment last) needs it, and
+    // half of the CTAs reach their item boundaries about half an item out
+    // of step with the other half, so the boundaries' bursts of new-context
+    // loads from HBM do not all fall at once.
+    if (tail_left && tail_jb > 0) {
+      f.item = tail_item;
+      f.jb = tail_jb;
+      f.je = tail_je;
+      tail_left = false;
+      return true;
+    }
     if (t < n_full) {
       f.item = t;
       f.jb = 0;
