@@ -30,21 +30,20 @@
 //            columns;  l += rowsum(P_j)
 //   MMA      O += P_j . V_j           A = P_j from TMEM, B = V_j from shared
 //                                     memory; M = 128, N = Dh, K = 128 keys
-// and finally O / l.  Q and P live in TMEM: with MMAs this small, operand
-// reads from shared memory rather than the tensor math set the pace
-// (measured on GB300: Q and P read from shared memory cost about half of
-// the kernel's time), so shared memory only feeds K and V.  TMEM holds Q
-// (64 columns of bf16 pairs), two S/P buffers of 128 columns and O (128).
+// and finally O / l.  P lives in TMEM (the A operand of PV); Q stays in
+// shared memory (the A operand of S), double-buffered over fragments.  TMEM
+// holds three S/P buffers of 128 columns and O (128), so S runs three blocks
+// ahead of PV.  Two threads issue the MMAs (S and PV), so that one
+// thread's barrier waits (each ~160 cycles while MMAs are in flight,
+// measured on GB300) overlap the other's products.
 // (128-key blocks: with 64 keys the N = 64 products ran at about half the
 // tensor rate and the per-block handshakes doubled.)
-// The issuer queues PV_{j-2} and then S_j, which overwrites the buffer
-// PV_{j-2} reads (the tensor core runs one thread's MMAs in issue order), so
-// S runs two blocks ahead of PV.  The softmax takes full blocks' scores in
-// pairs (three-input max, packed fp32x2 FMA and add): its instruction
-// stream, one warp per SM sub-partition, is what bounds the kernel.
-// Full 128-row tiles with bf16 output leave through the Q staging buffer
-// (free once the next item's Q is in TMEM) and TMA stores; ragged tiles and
-// fp32 output use direct stores.
+// S_j overwrites the buffer PV_{j-3} reads: the S issuer waits for PV_{j-3}
+// to complete first.
+// The softmax takes full blocks' scores in pairs (three-input max, packed
+// fp32x2 FMA and add).  Full 128-row tiles with bf16 output leave through
+// the fragment's Q buffer (free once its S products are done) and TMA
+// stores; ragged tiles and fp32 output use direct stores.
 //
 // Schedule: items are dealt round-robin to the persistent CTAs for as many
 // full waves as there are; the items of the last, partial wave (when it is
@@ -60,11 +59,12 @@
 // is resident.  (With 512 items on 152 SMs the last wave holds 56 items:
 // 84 % wave efficiency without the split.)
 //
-// Roles (256 threads): warp 0 TMA producer (Q once per item into a staging
-// buffer; K_j and V_j per block through separate 3-deep rings, since K_j is
-// consumed two blocks before V_j); warp 1 MMA issuer (one thread); warp 2
-// TMEM allocation; warp 3 lane 1 of CTA 0 validates the offsets; warps 4-7
-// copy Q into TMEM, run the softmax and write the output (thread = query
+// Roles (256 threads): warp 0 TMA producer of Q (once per item, into one of
+// two Q buffers) and K (3-deep ring); warp 3 lane 0 TMA producer of V (2-deep
+// ring: V_j is consumed three blocks after K_j); warp 1 issues the S
+// products and warp 2 the PV products (one thread each; warp 2 also
+// allocates the tensor memory); warp 3 lane 1 of CTA 0 validates the
+// offsets; warps 4-7 run the softmax and write the output (thread = query
 // row = TMEM lane).
 #pragma once
 
@@ -75,28 +75,30 @@ namespace wst {
 constexpr int kAttnDh = 128;          // head dimension (the MMA K of S, N of PV)
 constexpr int kAttnBM = 128;          // query rows per tile
 constexpr int kAttnBN = 128;          // keys per block
-constexpr int kAttnStages = 3;        // K ring and V ring depth (each)
+constexpr int kAttnKStages = 3;       // K ring depth
+constexpr int kAttnVStages = 2;       // V ring depth (V_j is read three blocks after K_j)
+constexpr int kAttnSBufs = 3;         // S/P buffers in TMEM: S runs three blocks ahead of PV
 constexpr int kAttnThreads = 256;
 constexpr int kAttnQBytes = kAttnBM * kAttnDh * 2;        // 32 KB: two 64-wide d halves
 constexpr int kAttnKBytes = kAttnBN * kAttnDh * 2;        // 32 KB: two 64-wide d halves
-// barriers: q_full, q_empty, qt_full, k_full[S], k_empty[S], v_full[S],
-// v_empty[S], s_full[2], p_full[2], pv_done[2], o_empty, o_staged,
-// merge_full[4] (one per softmax warp)
-constexpr int kAttnNumBars = 3 + 4 * kAttnStages + 12;
+// barriers: q_full[2], o_staged[2], k_full[KS], k_empty[KS], v_full[VS],
+// v_empty[VS], s_full[3], p_full[3], pv_done[3], o_empty, merge_full[4]
+// (one per softmax warp)
+constexpr int kAttnNumBars = 4 + 2 * kAttnKStages + 2 * kAttnVStages + 3 * kAttnSBufs + 5;
 // Users whose candidate offsets are copied into shared memory at the start
 // (the item walkers then read them there instead of through dependent
 // global loads); calls with more users read them from global memory.
 constexpr int kAttnSmemUsers = 256;
 constexpr size_t kAttnOffsBytes = (kAttnSmemUsers + 1) * 4 + 12;  // padded to 16 bytes
-constexpr size_t kAttnSmemBytes = (size_t)kAttnQBytes + 2 * (size_t)kAttnStages * kAttnKBytes +
+constexpr size_t kAttnSmemBytes = 2 * (size_t)kAttnQBytes +
+                                  (size_t)(kAttnKStages + kAttnVStages) * kAttnKBytes +
                                   512 /*barriers*/ + kAttnOffsBytes + 1024 /*align*/;
 static_assert(kAttnSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kAttnNumBars * 8 + 32 <= 512, "barrier area + TMEM slot, abort flag, item count");
-// TMEM columns: Q at 0 (64 columns of bf16 pairs), S/P buffers at 64 and
-// 192 (P as bf16 pairs in the first 64 columns of its S buffer), O at 320.
-constexpr int kAttnTmemQ = 0;
-constexpr int kAttnTmemS = 64;
-constexpr int kAttnTmemO = 320;
+// TMEM columns: S/P buffers at 0, 128 and 256 (P as bf16 pairs in the first
+// 64 columns of its S buffer), O at 384.  Q stays in shared memory.
+constexpr int kAttnTmemS = 0;
+constexpr int kAttnTmemO = kAttnSBufs * kAttnBN;
 static_assert(kAttnTmemO + kAttnDh <= 512, "TMEM columns");
 constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 
@@ -111,8 +113,8 @@ constexpr size_t kAttnSlotsOffset = kAttnFlagsOffset + (size_t)kAttnMaxCtas * 4 
 constexpr size_t kAttnSlotFloats = (size_t)kAttnDh * kAttnBM + 2 * kAttnBM;
 constexpr size_t kAttnWorkspaceBytes = kAttnSlotsOffset + (size_t)kAttnMaxCtas * kAttnSlotFloats * 4;
 constexpr int kAttnWarpPartBytes = kAttnDh * 32 * 4;        // 16 KB: one warp's O share
-constexpr int kAttnMergeBatch = 3;                           // partials staged per warp at a time
-static_assert(4 * kAttnMergeBatch * kAttnWarpPartBytes <= 2 * kAttnStages * kAttnKBytes,
+constexpr int kAttnMergeBatch = 2;                           // partials staged per warp at a time
+static_assert(4 * kAttnMergeBatch * kAttnWarpPartBytes <= (kAttnKStages + kAttnVStages) * kAttnKBytes,
               "merge staging fits in the K/V rings");
 
 // Bulk (TMA engine) copy of `bytes` contiguous bytes global -> shared,
@@ -403,10 +405,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                    // [2 halves][128 rows][64 d] staging
-  uint8_t* sK = sQ + kAttnQBytes;                        // [stage][2 d-halves][128 keys][64 d]
-  uint8_t* sV = sK + kAttnStages * kAttnKBytes;          // [stage][2 d-halves][128 keys][64 d]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnStages * kAttnKBytes);
+  uint8_t* sQ = smem;                                    // [2 bufs][2 halves][128 rows][64 d]
+  uint8_t* sK = sQ + 2 * kAttnQBytes;                    // [stage][2 d-halves][128 keys][64 d]
+  uint8_t* sV = sK + kAttnKStages * kAttnKBytes;         // [stage][2 d-halves][128 keys][64 d]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kAttnVStages * kAttnKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kAttnNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   long long* n_items_s = reinterpret_cast<long long*>(tmem_slot + 4);  // 8-byte aligned
@@ -416,40 +418,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t bar_base = smem_addr(bars);
-  const uint32_t q_full = bar_base;          // Q tile landed in the staging buffer
-  const uint32_t q_empty = bar_base + 8u;    // staging buffer copied into TMEM
-  const uint32_t qt_full = bar_base + 16u;   // Q in TMEM (4 softmax warps)
-  auto kf_bar = [&](int s) { return bar_base + 8u * (3 + s); };
-  auto ke_bar = [&](int s) { return bar_base + 8u * (3 + kAttnStages + s); };
-  auto vf_bar = [&](int s) { return bar_base + 8u * (3 + 2 * kAttnStages + s); };
-  auto ve_bar = [&](int s) { return bar_base + 8u * (3 + 3 * kAttnStages + s); };
-  auto sf_bar = [&](int b) { return bar_base + 8u * (3 + 4 * kAttnStages + b); };
-  auto pf_bar = [&](int b) { return bar_base + 8u * (5 + 4 * kAttnStages + b); };
-  auto pv_bar = [&](int b) { return bar_base + 8u * (7 + 4 * kAttnStages + b); };
-  const uint32_t oe_bar = bar_base + 8u * (9 + 4 * kAttnStages);
-  // o_staged: the 4 softmax warps are done with the Q staging buffer for a
-  // fragment's output (their TMA stores have read it); the producer waits
-  // for output k before loading the Q of fragment k + 2 there.
-  const uint32_t os_bar = bar_base + 8u * (10 + 4 * kAttnStages);
-  auto mg_bar = [&](int w) { return bar_base + 8u * (11 + 4 * kAttnStages + w); };
+  // q_full[qb]: fragment's Q tile landed in Q buffer qb (= fragment index & 1).
+  // o_staged[qb]: the 4 softmax warps are done with Q buffer qb for a
+  // fragment (its S products completed and its output's TMA stores, which
+  // stage through it, have read it); the producer waits for fragment k
+  // before loading the Q of fragment k + 2 there.
+  auto qf_bar = [&](int b) { return bar_base + 8u * b; };
+  auto os_bar = [&](int b) { return bar_base + 8u * (2 + b); };
+  auto kf_bar = [&](int s) { return bar_base + 8u * (4 + s); };
+  auto ke_bar = [&](int s) { return bar_base + 8u * (4 + kAttnKStages + s); };
+  auto vf_bar = [&](int s) { return bar_base + 8u * (4 + 2 * kAttnKStages + s); };
+  auto ve_bar = [&](int s) { return bar_base + 8u * (4 + 2 * kAttnKStages + kAttnVStages + s); };
+  constexpr int kSB0 = 4 + 2 * kAttnKStages + 2 * kAttnVStages;
+  auto sf_bar = [&](int b) { return bar_base + 8u * (kSB0 + b); };
+  auto pf_bar = [&](int b) { return bar_base + 8u * (kSB0 + kAttnSBufs + b); };
+  auto pv_bar = [&](int b) { return bar_base + 8u * (kSB0 + 2 * kAttnSBufs + b); };
+  const uint32_t oe_bar = bar_base + 8u * (kSB0 + 3 * kAttnSBufs);
+  auto mg_bar = [&](int w) { return bar_base + 8u * (kSB0 + 3 * kAttnSBufs + 1 + w); };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 4);
-    mbar_init(qt_full, 4);
-    for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(kf_bar(s), 1);
-      mbar_init(ke_bar(s), 1);
-      mbar_init(vf_bar(s), 1);
-      mbar_init(ve_bar(s), 1);
-    }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(qf_bar(b), 1);
+      mbar_init(os_bar(b), 4);
+    }
+    for (int st = 0; st < kAttnKStages; ++st) {
+      mbar_init(kf_bar(st), 1);
+      mbar_init(ke_bar(st), 1);
+    }
+    for (int st = 0; st < kAttnVStages; ++st) {
+      mbar_init(vf_bar(st), 1);
+      mbar_init(ve_bar(st), 1);
+    }
+    for (int b = 0; b < kAttnSBufs; ++b) {
       mbar_init(sf_bar(b), 1);
       mbar_init(pf_bar(b), 4);   // the 4 softmax warps
       mbar_init(pv_bar(b), 1);
     }
     mbar_init(oe_bar, 4);
-    mbar_init(os_bar, 4);
     for (int w4 = 0; w4 < 4; ++w4) mbar_init(mg_bar(w4), 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -476,23 +481,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t target = p.epoch;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ producer (Q and K)
+    // K_j is read by S_j, three blocks before PV_j reads V_j; with one
+    // thread loading both in order, a V slot freed late would hold back the
+    // next K load, so V has its own producer (warp 3).
     if (lane == 0) {
       AttnWalker w;
       w.init(p, offs);
       AttnSched sc;
       sc.init(n_items, nblk, p.split != 0);
       AttnFrag f;
-      int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0, it = 0;
+      int ks = 0;
+      uint32_t kph = 0, it = 0;
       bool ok = true;
       for (; ok && sc.next(f) && w.seek(p, f.item); ++it) {
         const AttnItem x = w.item(f.item);
-        if (!wait_phase(guard, q_empty, (it & 1u) ^ 1u, (kRoleProducer << 16) | 0x800)) break;
-        if (it >= 2 && !wait_phase(guard, os_bar, (it - 2u) & 1u, (kRoleProducer << 16) | 0x900)) break;
-        mbar_arrive_expect_tx(q_full, kAttnQBytes);
+        const int qb = (int)(it & 1u);
+        // Q buffer qb is free once fragment it - 2 is done with it
+        if (it >= 2 && !wait_phase(guard, os_bar(qb), ((it - 2u) >> 1) & 1u, (kRoleProducer << 16) | 0x900)) break;
+        mbar_arrive_expect_tx(qf_bar(qb), kAttnQBytes);
         for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem_addr(sQ + hf * (kAttnQBytes / 2)), &tmQ, q_full, hf * 64, x.h, x.row0);
+          tma_load_3d(smem_addr(sQ + qb * kAttnQBytes + hf * (kAttnQBytes / 2)), &tmQ, qf_bar(qb), hf * 64,
+                      x.h, x.row0);
         for (int j = f.jb; j < f.je; ++j) {
           if (!wait_phase(guard, ke_bar(ks), kph ^ 1u, (kRoleProducer << 16) | ks)) {
             ok = false;
@@ -502,53 +512,96 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int hf = 0; hf < 2; ++hf)
             attn_tma_load_4d(smem_addr(sK + ks * kAttnKBytes + hf * (kAttnKBytes / 2)), &tmK, kf_bar(ks),
                              hf * 64, x.h, j * kAttnBN, x.u);
-          if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
-          if (!wait_phase(guard, ve_bar(vs), vph ^ 1u, (kRoleProducer << 16) | 0x10 | vs)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(vf_bar(vs), kAttnKBytes);
-          for (int hf = 0; hf < 2; ++hf)
-            attn_tma_load_4d(smem_addr(sV + vs * kAttnKBytes + hf * (kAttnKBytes / 2)), &tmV, vf_bar(vs),
-                             hf * 64, x.h, j * kAttnBN, x.u);
-          if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
+          if (++ks == kAttnKStages) { ks = 0; kph ^= 1u; }
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 3 && lane == 0) {
+    // ------------------------------------------------------------------ producer (V)
+    AttnWalker w;
+    w.init(p, offs);
+    AttnSched sc;
+    sc.init(n_items, nblk, p.split != 0);
+    AttnFrag f;
+    int vs = 0;
+    uint32_t vph = 0;
+    bool ok = true;
+    while (ok && sc.next(f) && w.seek(p, f.item)) {
+      const AttnItem x = w.item(f.item);
+      for (int j = f.jb; j < f.je; ++j) {
+        if (!wait_phase(guard, ve_bar(vs), vph ^ 1u, (kRoleProducer << 16) | 0x10 | vs)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(vf_bar(vs), kAttnKBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          attn_tma_load_4d(smem_addr(sV + vs * kAttnKBytes + hf * (kAttnKBytes / 2)), &tmV, vf_bar(vs),
+                           hf * 64, x.h, j * kAttnBN, x.u);
+        if (++vs == kAttnVStages) { vs = 0; vph ^= 1u; }
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the S products, warp 2 the PV products (one thread
+    // each).  An mbarrier wait issued while the SM's tensor core works on
+    // MMAs takes ~160 cycles even when its phase completed long ago
+    // (measured on GB300); with one issuer, the waits of every key block
+    // left the tensor pipe idle, with two, one thread's MMAs run while the
+    // other waits.  S_j overwrites the buffer of P_{j-3}, so the S issuer
+    // first waits for PV_{j-3} to complete (three buffers: long done).
+    //   S = Q K^T: A = Q (shared memory, K-major over d: two 64-wide halves
+    //              16 KB apart, 16 d = 32 B per step), B = K_j (the same).
+    //   O += P V:  A = P (TMEM), B = V_j (MN-major: d contiguous, two 64-wide
+    //              d halves 16 KB apart, 16 keys = 2 KB per step).
     if (lane == 0) {
-      // S = Q K^T: A = Q (TMEM), B = K_j (K-major over d: two 64-wide halves
-      //            8 KB apart, 16 d = 32 B per step).
-      // O += P V:  A = P (TMEM), B = V_j (MN-major: d contiguous, two 64-wide
-      //            d halves 8 KB apart, 16 keys = 2 KB per step).
+      const bool s_role = warp == 1;
       constexpr uint32_t idesc_s = idesc_bf16_f32(kAttnBM, kAttnBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kAttnBM, kAttnDh, false, true);
-      const uint32_t a_q = tmem_base + kAttnTmemQ;
       const uint32_t d_o = tmem_base + kAttnTmemO;
       AttnSched sc;
       sc.init(n_items, nblk, p.split != 0);
       AttnFrag f;
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0, it = 0;
-      long long gb = 0;  // blocks before this fragment (buffer parity)
+      int sb = 0;            // S buffer of the next product (global block mod 3)
+      uint32_t sph = 0;      // ... and its use-count parity (global block / 3)
+      long long nprod = 0;   // products issued by this thread so far
       bool ok = true;
       for (; ok && sc.next(f); ++it) {
         const int nb = f.je - f.jb;
-        if (!wait_phase(guard, qt_full, it & 1u, (kRoleMma << 16) | 0x800)) break;
-        tc_fence_after_sync();
-        // Step j: PV_{j-2} (if j >= 2), then S_j (if j < nblk).  S_j
-        // overwrites the TMEM buffer that holds P_{j-2}; the tensor core
-        // performs this thread's MMAs in issue order, so PV_{j-2} reads P
-        // before S_j writes there (and PV_{j-2} waited for the softmax to
-        // finish block j-2, so S_{j-2} has been read as well).
-        for (int j = 0; j < nb + 2 && ok; ++j) {
-          if (j >= 2) {
-            const int jj = j - 2;
-            const long long g = gb + jj;
-            const int b = (int)(g & 1);
+        if (s_role) {
+          const int qb = (int)(it & 1u);
+          if (!wait_phase(guard, qf_bar(qb), (it >> 1) & 1u, (kRoleMma << 16) | 0x800)) break;
+          const uint32_t q_addr = smem_addr(sQ + qb * kAttnQBytes);
+          for (int j = 0; j < nb; ++j, ++nprod) {
+            const int b = sb;
+            // PV_{g-3} has read the P that S_g overwrites (use sph ^ 1 of
+            // this buffer: the previous use completed)
+            if (nprod >= kAttnSBufs && !wait_phase(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
+              ok = false;
+              break;
+            }
+            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t k_addr = smem_addr(sK + ks * kAttnKBytes);
+            const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
+#pragma unroll
+            for (int kk = 0; kk < kAttnDh / 16; ++kk) {
+              // 16 d: 32 B within a 64-wide half of Q and of K (16 KB apart)
+              const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
+              umma_bf16<1>(d_s, sdesc_sw128(q_addr + ko, 16, 1024), sdesc_sw128(k_addr + ko, 16, 1024),
+                           idesc_s, kk != 0 ? 1u : 0u);
+            }
+            umma_commit(sf_bar(b));
+            umma_commit(ke_bar(ks));
+            if (++ks == kAttnKStages) { ks = 0; kph ^= 1u; }
+            if (++sb == kAttnSBufs) { sb = 0; sph ^= 1u; }
+          }
+        } else {
+          for (int jj = 0; jj < nb; ++jj, ++nprod) {
+            const int b = sb;
             if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
-                !wait_phase(guard, pf_bar(b), (uint32_t)((g >> 1) & 1), (kRoleMma << 16) | 0x200 | b) ||
+                !wait_phase(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b) ||
                 (jj == 0 && !wait_phase(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
               ok = false;
               break;
@@ -562,66 +615,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                           (jj > 0 || kk != 0) ? 1u : 0u);
             umma_commit(pv_bar(b));
             umma_commit(ve_bar(vs));
-            if (++vs == kAttnStages) { vs = 0; vph ^= 1u; }
-          }
-          if (j < nb) {
-            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
-            tc_fence_after_sync();
-            const int b = (int)((gb + j) & 1);
-            const uint64_t kd0 = sdesc_sw128(smem_addr(sK + ks * kAttnKBytes), 16, 1024);
-            const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
-#pragma unroll
-            for (int kk = 0; kk < kAttnDh / 16; ++kk) {
-              // 16 d: 8 TMEM columns of Q; 32 B within a 64-wide half of K (16 KB apart)
-              const uint32_t ko = (uint32_t)((kk >> 2) * (kAttnKBytes / 2) + (kk & 3) * 32);
-              attn_mma_ts(d_s, a_q + (uint32_t)(kk * 8), kd0 + (ko >> 4), idesc_s, kk != 0 ? 1u : 0u);
-            }
-            umma_commit(sf_bar(b));
-            umma_commit(ke_bar(ks));
-            if (++ks == kAttnStages) { ks = 0; kph ^= 1u; }
+            if (++vs == kAttnVStages) { vs = 0; vph ^= 1u; }
+            if (++sb == kAttnSBufs) { sb = 0; sph ^= 1u; }
           }
         }
-        gb += nb;
       }
     }
   } else if (warp == 3) {
     if (lane == 1 && blockIdx.x == 0) attn_check_offsets(p);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------------ Q copy, softmax, output
+    // ------------------------------------------------------------------ softmax, output
     const int q = warp & 3;
     const int row = q * 32 + (int)lane;  // query row of the tile = TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16);
     const uint32_t t_o = t_lane + kAttnTmemO;
-    // Q row of item `it` -> TMEM (64 columns of bf16 pairs), then release
-    // the staging buffer and tell the MMA issuer.
-    auto copy_q = [&](uint32_t it) -> bool {
-      if (!warp_wait_phase(guard, q_full, it & 1u, (kRoleEpilogue << 16) | 0x400)) return false;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float qv[32];
-        const uint32_t qrow = smem_addr(sQ + hf * (kAttnQBytes / 2)) + (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
-          uint32_t a, b2, c2, d;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(a), "=r"(b2), "=r"(c2), "=r"(d)
-                       : "r"(qrow + (uint32_t)(((c ^ (row & 7)) & 7) * 16)));
-          qv[4 * c + 0] = __uint_as_float(a);
-          qv[4 * c + 1] = __uint_as_float(b2);
-          qv[4 * c + 2] = __uint_as_float(c2);
-          qv[4 * c + 3] = __uint_as_float(d);
-        }
-        attn_tmem_store32(t_lane + kAttnTmemQ + hf * 32, qv);
-      }
-      attn_tmem_store_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(q_empty);
-        mbar_arrive(qt_full);
-      }
-      return true;
-    };
     AttnWalker w;
     w.init(p, offs);
     AttnSched sc;
@@ -638,16 +645,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       pending_release = false;
     };
-    bool ok = sc.next(f) && w.seek(p, f.item) && copy_q(0);
+    // S buffer and use-count parity of the next block (global block index
+    // mod 3, and / 3), and of the previous block
+    int sbuf = 0, pbuf = 0;
+    uint32_t sphase = 0, pphase = 0;
+    bool ok = sc.next(f) && w.seek(p, f.item);
     while (ok) {
       const AttnItem x = w.item(f.item);
       const int nb = f.je - f.jb;
+      const int qb = (int)(it & 1u);  // this fragment's Q buffer (also its output staging)
       float m = -INFINITY, l = 0.0f;
       for (int jr = 0; jr < nb; ++jr) {
         const int j = f.jb + jr;  // key block within the context
-        const long long g = gb + jr;
-        const int b = (int)(g & 1);
-        const uint32_t ph = (uint32_t)((g >> 1) & 1);
+        const int b = sbuf;
+        const uint32_t ph = sphase;
         if (!warp_wait_phase(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
         tc_fence_after_sync();
         float s[kAttnBN];
@@ -690,8 +701,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (__any_sync(0xffffffffu, grow)) {
             // O holds the PV products of blocks < j: wait for the last one,
             // then rescale O and l of the rows whose maximum grew.
-            const long long gp = g - 1;
-            if (!warp_wait_phase(guard, pv_bar((int)(gp & 1)), (uint32_t)((gp >> 1) & 1),
+            if (!warp_wait_phase(guard, pv_bar(pbuf), pphase,
                                  (kRoleEpilogue << 16) | 0x100)) { ok = false; break; }
             tc_fence_after_sync();
             const float alpha = grow ? attn_ex2(m - mx) : 1.0f;
@@ -747,19 +757,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(pf_bar(b));
         if (pending_release) release_partial();
+        pbuf = b;
+        pphase = ph;
+        if (++sbuf == kAttnSBufs) { sbuf = 0; sphase ^= 1u; }
       }
       if (!ok) break;
-      // Bring the next fragment's Q into TMEM before this one's output, so
-      // its first S products overlap the epilogue.  Every S product of this
-      // fragment (the readers of Q in TMEM) completed before the last s_full.
       AttnFrag fn;
       const bool more = sc.next(fn) && w.seek(p, fn.item);
       ++it;
-      if (more && !copy_q(it)) break;
-      // Output: wait for the last PV product, then one of three ends.
-      const long long gl = gb + nb - 1;
-      if (!warp_wait_phase(guard, pv_bar((int)(gl & 1)), (uint32_t)((gl >> 1) & 1),
-                           (kRoleEpilogue << 16) | 0x300)) { ok = false; break; }
+      // Output: wait for the last PV product (the products of one thread
+      // complete in order, so this fragment's S products, the readers of its
+      // Q buffer, are done too), then one of three ends.
+      if (!warp_wait_phase(guard, pv_bar(pbuf), pphase, (kRoleEpilogue << 16) | 0x300)) { ok = false; break; }
       tc_fence_after_sync();
       gb += nb;
       const bool store = row < x.rows;
@@ -781,7 +790,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
         }
       };
-      // Full bf16 tiles leave through the Q staging buffer and TMA; the
+      // Full bf16 tiles leave through the fragment's Q buffer and TMA; the
       // rest (fp32 output, ragged tiles that must not touch the next
       // user's rows) through direct stores.
       const bool tma_out = !OUT_F32 && x.rows == kAttnBM;
@@ -789,7 +798,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (tma_out) {
           // 32 columns = 64 B of the row, in d-half c/2 at byte (c%2)*64:
           // 16-byte units (c%2)*4 .. +3, 128-byte swizzle as the Q tile.
-          const uint32_t rb = smem_addr(sQ) + (uint32_t)((c >> 1) * (kAttnQBytes / 2) + row * 128);
+          const uint32_t rb = smem_addr(sQ + qb * kAttnQBytes) + (uint32_t)((c >> 1) * (kAttnQBytes / 2) + row * 128);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const uint32_t unit = (uint32_t)((c & 1) * 4 + jj);
@@ -849,11 +858,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           return -1;
         };
+        static_assert(kAttnMergeBatch == 2 || kAttnMergeBatch == 3, "merge batch of 2 or 3");
         int cs0 = -1, cs1 = -1, cs2 = -1, nbat = 0;
         auto collect = [&]() {
           cs0 = next_partial();
           cs1 = cs0 >= 0 ? next_partial() : -1;
-          cs2 = cs1 >= 0 ? next_partial() : -1;
+          cs2 = kAttnMergeBatch > 2 && cs1 >= 0 ? next_partial() : -1;
           nbat = (cs0 >= 0) + (cs1 >= 0) + (cs2 >= 0);
         };
         collect();
@@ -976,13 +986,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) {
         mbar_arrive(oe_bar);
         if (staged) {
-          const uint32_t sb = smem_addr(sQ) + (uint32_t)(q * 32 * 128);
+          const uint32_t sb = smem_addr(sQ + qb * kAttnQBytes) + (uint32_t)(q * 32 * 128);
           tma_store_3d(&tmO, sb, 0, x.h, x.row0 + q * 32);
           tma_store_3d(&tmO, sb + kAttnQBytes / 2, 64, x.h, x.row0 + q * 32);
           bulk_commit_group();
           bulk_wait_group_read<0>();
         }
-        mbar_arrive(os_bar);
+        mbar_arrive(os_bar(qb));
       }
       if (!more) break;
       f = fn;
