@@ -101,6 +101,11 @@ constexpr int kAttnTmemS = 0;
 constexpr int kAttnTmemO = kAttnSBufs * kAttnBN;
 static_assert(kAttnTmemO + kAttnDh <= 512, "TMEM columns");
 constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr float kAttnRescaleBound = 256.0f;  // 2^kAttnRescaleLog2: the largest P kept
+#ifndef WST_ATTN_EARLY_TEST
+#define WST_ATTN_EARLY_TEST 40
+#endif
+constexpr int kAttnEarlyTestPair = WST_ATTN_EARLY_TEST;  // score pair of a full block at which the next S is tested
 
 // Stream-K workspace after the 256-byte header: uint32 flags[kAttnMaxCtas][4]
 // (one per softmax warp), then one partial slot per CTA: O as [4 warps][Dh/4
@@ -577,11 +582,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int b = sb;
             // PV_{g-3} has read the P that S_g overwrites (use sph ^ 1 of
             // this buffer: the previous use completed)
-            if (nprod >= kAttnSBufs && !wait_phase(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
+            if (nprod >= kAttnSBufs && !wait_phase_spin(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
               ok = false;
               break;
             }
-            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
+            if (!wait_phase_spin(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
             tc_fence_after_sync();
             const uint32_t k_addr = smem_addr(sK + ks * kAttnKBytes);
             const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
@@ -600,9 +605,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         } else {
           for (int jj = 0; jj < nb; ++jj, ++nprod) {
             const int b = sb;
-            if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
-                !wait_phase(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b) ||
-                (jj == 0 && !wait_phase(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
+            if (!wait_phase_spin(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
+                !wait_phase_spin(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b) ||
+                (jj == 0 && !wait_phase_spin(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
               ok = false;
               break;
             }
@@ -637,6 +642,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     long long gb = 0;
     uint32_t it = 0;
     bool pending_release = false;  // published a partial, flag not yet released
+    int pending_os = -1;           // Q buffer whose staged output a TMA store may still read
     uint32_t mg_phase = 0;         // merge batches this warp has staged
     auto release_partial = [&]() {
       if (lane == 0) {
@@ -649,6 +655,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // mod 3, and / 3), and of the previous block
     int sbuf = 0, pbuf = 0;
     uint32_t sphase = 0, pphase = 0;
+    // The next block's S product was seen complete by an early test during
+    // this block's exponentials (each lane's test acquires it), so its wait
+    // can be skipped: a wait on a completed phase still costs ~160 cycles
+    // while MMAs are in flight, on the softmax's critical path.
+    bool s_ready = false;
     bool ok = sc.next(f) && w.seek(p, f.item);
     while (ok) {
       const AttnItem x = w.item(f.item);
@@ -659,86 +670,136 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int j = f.jb + jr;  // key block within the context
         const int b = sbuf;
         const uint32_t ph = sphase;
-        if (!warp_wait_phase(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, s_ready) &&
+            !warp_wait_phase_spin(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
+        s_ready = false;
         tc_fence_after_sync();
+        // the block after this one: its S buffer and use-count parity
+        const int b_next = b + 1 == kAttnSBufs ? 0 : b + 1;
+        const uint32_t ph_next = b + 1 == kAttnSBufs ? ph ^ 1u : ph;
         float s[kAttnBN];
 #pragma unroll
         for (int c = 0; c < kAttnBN / 32; ++c)
           tmem_load32(t_lane + kAttnTmemS + kAttnBN * b + 32 * c, *reinterpret_cast<float(*)[32]>(s + 32 * c));
-        // Row extremum of the raw scores (the maximum of cs * s is cs * max s
-        // for cs >= 0 and cs * min s otherwise); keys past the end of the
-        // context (last block only) take no part and get no weight.
         const int kvalid = p.Lkv - j * kAttnBN;
         const float cs = p.scale_log2;
         const bool pos = cs >= 0.0f;
+        // Row extremum of the raw scores (the maximum of cs * s is cs * max s
+        // for cs >= 0 and cs * min s otherwise), scores 2i, 2i+1 going to
+        // accumulator i % 8; keys past the end of the context (last block
+        // only) take no part and get no weight.
         float e8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) e8[i] = pos ? -INFINITY : INFINITY;
-        if (kvalid >= kAttnBN) {
-          // scores 2i, 2i+1 go to accumulator i % 8
-          if (pos) {
-#pragma unroll
-            for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_max3(e8[i & 7], s[2 * i], s[2 * i + 1]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_min3(e8[i & 7], s[2 * i], s[2 * i + 1]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < kAttnBN; ++i)
-            if (i < kvalid) e8[i & 7] = pos ? fmaxf(e8[i & 7], s[i]) : fminf(e8[i & 7], s[i]);
-        }
-        float ext;
-        if (pos)
-          ext = fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])), fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])));
-        else
-          ext = fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
-        const float mx = ext * cs;
-        if (jr == 0) {
-          m = mx;  // the first PV product overwrites O: nothing to rescale
-        } else {
-          const bool grow = mx > m + kAttnRescaleLog2;
-          if (__any_sync(0xffffffffu, grow)) {
-            // O holds the PV products of blocks < j: wait for the last one,
-            // then rescale O and l of the rows whose maximum grew.
-            if (!warp_wait_phase(guard, pv_bar(pbuf), pphase,
-                                 (kRoleEpilogue << 16) | 0x100)) { ok = false; break; }
-            tc_fence_after_sync();
-            const float alpha = grow ? attn_ex2(m - mx) : 1.0f;
-            if (grow) {
-              l *= alpha;
-              m = mx;
-            }
-#pragma unroll
-            for (int c = 0; c < kAttnDh / 32; ++c) {
-              float v[32];
-              tmem_load32(t_o + c * 32, v);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= alpha;
-              attn_tmem_store32(t_o + c * 32, v);
-            }
-            attn_tmem_store_wait();
-          }
-        }
-        // P = 2^(cs * s - m), one FFMA and one ex2 per score.
+        auto extremum = [&]() -> float {
+          const float ext =
+              pos ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])), fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
+                  : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
+          return ext * cs;
+        };
+        // P = 2^(cs * s - m), one FFMA and one ex2 per score; for full
+        // blocks in pairs (one packed FFMA and one packed add per two
+        // scores; score e sums into rs8[e % 8]).
         float rs8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rs8[i] = 0.0f;
-        if (kvalid >= kAttnBN) {
-          // pairs: one packed FFMA and one packed add per two scores; score
-          // e still sums into rs8[e % 8]
+        bool p_done = false;  // s holds P_j and rs8 its row sums
+        float mx;
+        if (kvalid >= kAttnBN && jr > 0) {
+          // After a fragment's first block the maximum rarely needs to grow
+          // (only when some score exceeds m by more than 2^8), so the
+          // exponentials run with the current m and no extremum is taken:
+          // every P is >= 0, so a row sum of at most 2^8 proves that no P of
+          // the row exceeds 2^8, i.e. that m need not grow, exactly the
+          // test the extremum would make.  (The special-function, FMA and
+          // comparison instructions share the sub-partition's dispatch, so
+          // the comparisons saved are time saved.)  Only when some row's sum
+          // is larger (or not finite) is S_j, still in TMEM, reloaded and the
+          // general path taken.
 #pragma unroll
           for (int i = 0; i < kAttnBN / 2; ++i) {
+            if (i == kAttnEarlyTestPair) s_ready = mbar_test_wait(sf_bar(b_next), ph_next);
             attn_fma2(s[2 * i], s[2 * i + 1], cs, -m);
             s[2 * i] = attn_ex2(s[2 * i]);
             s[2 * i + 1] = attn_ex2(s[2 * i + 1]);
             attn_add2(rs8[2 * (i & 3)], rs8[2 * (i & 3) + 1], s[2 * i], s[2 * i + 1]);
           }
-        } else {
+          const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+          if (__any_sync(0xffffffffu, !(rs <= kAttnRescaleBound))) {
 #pragma unroll
-          for (int i = 0; i < kAttnBN; ++i) {
-            s[i] = i < kvalid ? attn_ex2(fmaf(s[i], cs, -m)) : 0.0f;
-            rs8[i & 7] += s[i];
+            for (int c = 0; c < kAttnBN / 32; ++c)
+              tmem_load32(t_lane + kAttnTmemS + kAttnBN * b + 32 * c, *reinterpret_cast<float(*)[32]>(s + 32 * c));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rs8[i] = 0.0f;
+            if (pos) {
+#pragma unroll
+              for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_max3(e8[i & 7], s[2 * i], s[2 * i + 1]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_min3(e8[i & 7], s[2 * i], s[2 * i + 1]);
+            }
+            mx = extremum();
+          } else {
+            p_done = true;
+          }
+        } else {
+          if (kvalid >= kAttnBN) {
+            if (pos) {
+#pragma unroll
+              for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_max3(e8[i & 7], s[2 * i], s[2 * i + 1]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < kAttnBN / 2; ++i) e8[i & 7] = attn_min3(e8[i & 7], s[2 * i], s[2 * i + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kAttnBN; ++i)
+              if (i < kvalid) e8[i & 7] = pos ? fmaxf(e8[i & 7], s[i]) : fminf(e8[i & 7], s[i]);
+          }
+          mx = extremum();
+        }
+        if (!p_done) {
+          if (jr == 0) {
+            m = mx;  // the first PV product overwrites O: nothing to rescale
+          } else {
+            const bool grow = mx > m + kAttnRescaleLog2;
+            if (__any_sync(0xffffffffu, grow)) {
+              // O holds the PV products of blocks < j: wait for the last one,
+              // then rescale O and l of the rows whose maximum grew.
+              if (!warp_wait_phase(guard, pv_bar(pbuf), pphase,
+                                   (kRoleEpilogue << 16) | 0x100)) { ok = false; break; }
+              tc_fence_after_sync();
+              const float alpha = grow ? attn_ex2(m - mx) : 1.0f;
+              if (grow) {
+                l *= alpha;
+                m = mx;
+              }
+#pragma unroll
+              for (int c = 0; c < kAttnDh / 32; ++c) {
+                float v[32];
+                tmem_load32(t_o + c * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                attn_tmem_store32(t_o + c * 32, v);
+              }
+              attn_tmem_store_wait();
+            }
+          }
+          if (kvalid >= kAttnBN) {
+#pragma unroll
+            for (int i = 0; i < kAttnBN / 2; ++i) {
+              if (i == kAttnEarlyTestPair) s_ready = mbar_test_wait(sf_bar(b_next), ph_next);
+              attn_fma2(s[2 * i], s[2 * i + 1], cs, -m);
+              s[2 * i] = attn_ex2(s[2 * i]);
+              s[2 * i + 1] = attn_ex2(s[2 * i + 1]);
+              attn_add2(rs8[2 * (i & 3)], rs8[2 * (i & 3) + 1], s[2 * i], s[2 * i + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kAttnBN; ++i) {
+              s[i] = i < kvalid ? attn_ex2(fmaf(s[i], cs, -m)) : 0.0f;
+              rs8[i & 7] += s[i];
+            }
           }
         }
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
@@ -757,6 +818,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(pf_bar(b));
         if (pending_release) release_partial();
+        if (pending_os >= 0) {
+          // The previous fragment's output stores have long read their
+          // staging by now: release the Q buffer to the producer.
+          if (lane == 0) {
+            bulk_wait_group_read<0>();
+            mbar_arrive(os_bar(pending_os));
+          }
+          pending_os = -1;
+        }
         pbuf = b;
         pphase = ph;
         if (++sbuf == kAttnSBufs) { sbuf = 0; sphase ^= 1u; }
@@ -990,10 +1060,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_store_3d(&tmO, sb, 0, x.h, x.row0 + q * 32);
           tma_store_3d(&tmO, sb + kAttnQBytes / 2, 64, x.h, x.row0 + q * 32);
           bulk_commit_group();
-          bulk_wait_group_read<0>();
+        } else {
+          mbar_arrive(os_bar(qb));
         }
-        mbar_arrive(os_bar(qb));
       }
+      // A staged buffer is released after the next fragment's first block
+      // (waiting here for the stores to read it held the softmax at every
+      // item boundary); the producer needs it only for the Q after next.
+      if (staged) pending_os = qb;
       if (!more) break;
       f = fn;
     }
