@@ -582,11 +582,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int b = sb;
             // PV_{g-3} has read the P that S_g overwrites (use sph ^ 1 of
             // this buffer: the previous use completed)
-            if (nprod >= kAttnSBufs && !wait_phase_spin(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
+            if (nprod >= kAttnSBufs && !wait_phase(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
               ok = false;
               break;
             }
-            if (!wait_phase_spin(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
+            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
             tc_fence_after_sync();
             const uint32_t k_addr = smem_addr(sK + ks * kAttnKBytes);
             const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
@@ -605,9 +605,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         } else {
           for (int jj = 0; jj < nb; ++jj, ++nprod) {
             const int b = sb;
-            if (!wait_phase_spin(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
-                !wait_phase_spin(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b) ||
-                (jj == 0 && !wait_phase_spin(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
+            if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
+                !wait_phase(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b) ||
+                (jj == 0 && !wait_phase(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
               ok = false;
               break;
             }
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int b = sbuf;
         const uint32_t ph = sphase;
         if (!__all_sync(0xffffffffu, s_ready) &&
-            !warp_wait_phase_spin(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
+            !warp_wait_phase(guard, sf_bar(b), ph, (kRoleEpilogue << 16) | b)) { ok = false; break; }
         s_ready = false;
         tc_fence_after_sync();
         // the block after this one: its S buffer and use-count parity

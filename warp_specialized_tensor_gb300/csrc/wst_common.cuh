@@ -86,46 +86,11 @@ __device__ __forceinline__ bool wait_phase_cluster(const Guard& g, uint32_t bar,
   return wait_slow(g, bar, parity, info, true);
 }
 
-// The same wait spinning on the non-suspending test, for waits on a
-// kernel's critical path: a thread suspended in mbarrier.try_wait was seen
-// (GB300, clock stamps) to resume up to ~500 cycles after the phase
-// completed.  Bounded like wait_slow.
-static __device__ __noinline__ bool wait_spin_slow(const Guard& g, uint32_t bar, uint32_t parity,
-                                            uint32_t info) {
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t it = 0;
-  while (!mbar_test_wait(bar, parity)) {
-    if ((++it & 63u) == 0u) {
-      if (*g.abort) return false;
-      if (globaltimer_ns() - t0 > g.limit_ns || it > (1u << 30)) {
-        *g.abort = 1u;
-        latch_error(g.ws, kErrTimeout, info);
-        return false;
-      }
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ bool wait_phase_spin(const Guard& g, uint32_t bar, uint32_t parity,
-                                                uint32_t info) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return wait_spin_slow(g, bar, parity, info);
-}
-
 // Warp-collective form: lane 0 waits, the outcome is broadcast to the warp.
 __device__ __forceinline__ bool warp_wait_phase(const Guard& g, uint32_t bar, uint32_t parity,
                                                 uint32_t info) {
   uint32_t ok = 0;
   if (lane_id() == 0) ok = wait_phase(g, bar, parity, info) ? 1u : 0u;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool warp_wait_phase_spin(const Guard& g, uint32_t bar, uint32_t parity,
-                                                     uint32_t info) {
-  uint32_t ok = 0;
-  if (lane_id() == 0) ok = wait_phase_spin(g, bar, parity, info) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
 }
