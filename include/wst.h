@@ -100,9 +100,10 @@ typedef enum {
  *                             hardware cluster launch control).
  *   WST_OPT_DENSE_CTA_GROUP   tile shape of the dense, batched and
  *                             norm-fused GEMMs: 0 automatic (default: CTA
- *                             pairs on 256-row tiles when M > 128, else one
- *                             CTA per 128-row tile), 1 always one CTA per
- *                             128-row tile, 2 always CTA pairs.
+ *                             pairs on 256-row tiles when M > 128 and
+ *                             K > 512, else one CTA per 128-row tile), 1
+ *                             always one CTA per 128-row tile, 2 always CTA
+ *                             pairs.
  *   WST_OPT_IKBO_SCHEDULE     candidate schedule of the IKBO linear
  *                             compression (both entry points):
  *                             WST_SCHED_STATIC (default: a persistent grid,
@@ -165,7 +166,7 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K,
  * for Production ML at Scale", companion work on norm fusion into GEMMs, and
  * "Five key areas": model-aware fusion); the pages give no formula, this is
  * the plainest RMSNorm reading.  Runs on 256 x 256 CTA-pair tiles when
- * M > 128, else on single-CTA 128 x 256 tiles.
+ * M > 128 and K > 512, else on single-CTA 128 x 256 tiles.
  */
 wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
                                  const void* A, long lda, long strideA,

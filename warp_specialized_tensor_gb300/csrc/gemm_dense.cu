@@ -15,12 +15,19 @@ constexpr int kBN = 256;
 template <int CG>
 constexpr int stages_for() { return CG == 2 ? 6 : 4; }
 
-// CTA-pair tiles for dense problems with more than one 128-row block, unless
-// the process-wide option WST_OPT_DENSE_CTA_GROUP forces a choice.
-inline int dense_cta_group(int M) {
+// CTA-pair tiles for dense problems with more than one 128-row block and
+// more than 8 K-blocks, unless the process-wide option
+// WST_OPT_DENSE_CTA_GROUP forces a choice.  With 8 K-blocks or fewer the
+// pair's per-tile coupling (the leader's MMAs wait for both CTAs' loads,
+// both epilogues release the accumulator) outweighs the halved B traffic:
+// measured on GB300 with bias + SiLU, 512 x (1024 x 256 x 512) ran 0.148 ms
+// on single CTAs against 0.178 ms on pairs, while from K = 1024 up pairs
+// won (256 x (1024 x 256 x 1024): 0.129 vs 0.136 ms; 8192^3: 0.612 vs
+// 0.691 ms).
+inline int dense_cta_group(int M, int K) {
   const int forced = option_value(OPT_DENSE_CTA_GROUP);
   if (forced == 1 || forced == 2) return forced;
-  return M > kBM ? 2 : 1;
+  return M > kBM && K > 8 * kBK ? 2 : 1;
 }
 
 template <bool OUT_F32, int EPI, int CG, int NORM>
@@ -216,7 +223,7 @@ int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   int st = current_device_info(&dev);
   if (st) return st;
   if (pr.grouped) return run_gemm_grouped(pr, dev, stream);
-  const bool pair = dense_cta_group(pr.M) == 2;
+  const bool pair = dense_cta_group(pr.M, pr.K) == 2;
   if (pr.norm == 1) return pair ? dispatch<2, 1>(pr, dev, stream) : dispatch<1, 1>(pr, dev, stream);
   if (pr.norm == 2) return pair ? dispatch<2, 2>(pr, dev, stream) : dispatch<1, 2>(pr, dev, stream);
   return pair ? dispatch<2, 0>(pr, dev, stream) : dispatch<1, 0>(pr, dev, stream);
