@@ -661,8 +661,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // while MMAs are in flight, on the softmax's critical path.
     bool s_ready = false;
     bool ok = sc.next(f) && w.seek(p, f.item);
+    AttnItem x_next = ok ? w.item(f.item) : AttnItem{};
     while (ok) {
-      const AttnItem x = w.item(f.item);
+      const AttnItem x = x_next;
       const int nb = f.je - f.jb;
       const int qb = (int)(it & 1u);  // this fragment's Q buffer (also its output staging)
       float m = -INFINITY, l = 0.0f;
@@ -802,6 +803,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
         }
+        // a second early test (the first finds S_{j+1} complete in under half
+        // of the blocks), its latency covered by the packing below
+        if (!s_ready) s_ready = mbar_test_wait(sf_bar(b_next), ph_next);
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         // P_j -> TMEM as bf16 pairs over the first 64 columns of S_j's buffer
         // (the A operand of the PV product), then hand it to the MMA issuer.
@@ -834,7 +838,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       AttnFrag fn;
       const bool more = sc.next(fn) && w.seek(p, fn.item);
+      if (more) x_next = w.item(fn.item);
       ++it;
+      const float inv_l = 1.0f / l;  // of a whole item (a merged one computes its own)
       // Output: wait for the last PV product (the products of one thread
       // complete in order, so this fragment's S products, the readers of its
       // Q buffer, are done too), then one of three ends.
@@ -1038,15 +1044,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         staged = tma_out;
-      } else {
-        const float inv = 1.0f / l;
+      } else if (tma_out) {
+        // The whole item: its rows, normalised, into the Q buffer's 128-byte
+        // swizzle (written out directly: through the emit_chunk helper this
+        // path took ~1400 cycles, GB300 clock stamps).
+        const float inv = inv_l;
+        const uint32_t rb0 = smem_addr(sQ + qb * kAttnQBytes) + (uint32_t)(row * 128);
 #pragma unroll
         for (int c = 0; c < kAttnDh / 32; ++c) {
           float v[32];
           tmem_load32(t_o + c * 32, v);
-          emit_chunk(c, v, inv);
+          const uint32_t rb = rb0 + (uint32_t)((c >> 1) * (kAttnQBytes / 2));
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t unit = (uint32_t)((c & 1) * 4 + jj);
+            st_shared_v4(rb + ((unit ^ (uint32_t)(row & 7)) << 4),
+                         pack_bf16x2(v[8 * jj] * inv, v[8 * jj + 1] * inv),
+                         pack_bf16x2(v[8 * jj + 2] * inv, v[8 * jj + 3] * inv),
+                         pack_bf16x2(v[8 * jj + 4] * inv, v[8 * jj + 5] * inv),
+                         pack_bf16x2(v[8 * jj + 6] * inv, v[8 * jj + 7] * inv));
+          }
         }
-        staged = tma_out;
+        staged = true;
+      } else {
+#pragma unroll
+        for (int c = 0; c < kAttnDh / 32; ++c) {
+          float v[32];
+          tmem_load32(t_o + c * 32, v);
+          store_chunk(c, v, inv_l);
+        }
       }
       // O has been read: free it for the next fragment's PV products, then
       // store the staged rows (if any) and release the staging buffer.
