@@ -150,6 +150,27 @@ def test_attention_rescale_path(wst):
         check(O, ref, d["V"], out == torch.bfloat16, what="rescale")
 
 
+def test_attention_large_row_sum_without_growth(wst):
+    # After a fragment's first block the kernel skips the row maximum while
+    # the block's row sum stays <= 2^8; here every later key scores ~6.0
+    # (base 2) above the first block's maximum, so the sums are ~128 x 2^6
+    # while no single weight exceeds 2^8: the kernel must take its reload
+    # path, find that the maximum need not grow, and still produce the exact
+    # softmax (weights 1 in the first block, ~2^6 after it).
+    d = synthetic.ikbo_attention(users=2, cand_per_user=[70, 9], Lq=2, H=2, Lkv=520, seed=10)
+    Q = torch.zeros(d["Q"].shape)
+    Q[..., 0] = 1.0
+    K = torch.zeros(d["K"].shape)
+    K[:, 128:, :, 0] = 6.0 / math.log2(math.e)  # raw score 4.16: 2^(log2(e) * 4.16) ~ 2^6
+    K[:, 300:310, :, 0] = -3.0                   # and a few low ones
+    d["Q"], d["K"] = Q.to(torch.bfloat16), K.to(torch.bfloat16)
+    for out in (torch.float32, torch.bfloat16):
+        O, st = run(wst, d, out, scale=1.0)
+        assert st == 0
+        ref = oracle.ikbo_attention(d["Q"], d["K"], d["V"], d["user_offsets"], 2, scale=1.0)
+        check(O, ref, d["V"], out == torch.bfloat16, what="large row sums")
+
+
 @pytest.mark.parametrize("scale", [-0.3, 0.0])
 def test_attention_negative_and_zero_scale(wst, scale):
     # scale < 0: the row extremum is the minimum of the raw scores; scale = 0:
