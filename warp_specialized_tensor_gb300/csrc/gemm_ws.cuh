@@ -219,9 +219,11 @@ struct GemmCfg {
 // lane one row: eight 16-byte swizzled chunks per stage), accumulate the
 // row's sum of squares in fp32, release the stage together with the MMA, and
 // hand 1/sqrt(ss/K + eps) per row to the epilogue through a double-buffered
-// shared array.  The norm costs no extra pass over A in HBM.  The stats
-// warps read a stage after the MMAs that use it: the MMA issuer's per-stage
-// commit goes to consumed[s] (in both CTAs of a pair, by the commit's
+// shared array.  The norm costs no extra pass over A in HBM.  On a single
+// CTA the stats warps read a stage as soon as it lands (full[s]), alongside
+// the MMAs, and empty[s] needs both the MMA commit and the stats warps.  On
+// a CTA pair they read it after the MMAs that use it: the MMA issuer's
+// per-stage commit goes to consumed[s] (in both CTAs, by the commit's
 // multicast) instead of empty[s], and the stats warps release empty[s] once
 // they have read the stage.  (In a pair, both CTAs' loads complete on the
 // leader's full[s], which the peer's warps cannot wait on; relaying full[s]
@@ -270,9 +272,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      // released by the MMA commit, or (NORM) by the stats warps, which wait
-      // for the MMA commit on consumed[s]
-      mbar_init(empty_bar(s), NORM ? Cfg::kStatsWarps : 1);
+      // released by the MMA commit; with the row statistics, on CTA pairs
+      // by the stats warps, which wait for the MMA commit on consumed[s],
+      // and on single CTAs by both (the stats warps read the stage as soon
+      // as it lands, alongside the MMAs)
+      mbar_init(empty_bar(s), !NORM ? 1 : (CG == 1 ? 1 + Cfg::kStatsWarps : Cfg::kStatsWarps));
       mbar_init(cons_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -383,8 +387,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           // slot free (in both CTAs) once these MMAs finish; with the row
-          // statistics, once the stats warps have read it after them
-          const uint32_t rel = NORM ? cons_bar(stage) : empty_bar(stage);
+          // statistics, once the stats warps have read it too (on a pair,
+          // after these MMAs)
+          const uint32_t rel = (NORM && CG == 2) ? cons_bar(stage) : empty_bar(stage);
           if constexpr (CG == 1) umma_commit(rel);
           else                   umma_commit_pair(rel, 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -418,9 +423,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       float c = 0.0f;
       uint64_t negc2 = 0;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        // the MMAs that read this stage completed (their commit, multicast
-        // to both CTAs of a pair, arrives on consumed[s])
-        const uint32_t ready = cons_bar(stage);
+        // On a pair: the MMAs that read this stage completed (their commit,
+        // multicast to both CTAs, arrives on consumed[s]; the peer cannot
+        // wait on the leader's full[s]).  On a single CTA: the stage landed.
+        const uint32_t ready = CG == 2 ? cons_bar(stage) : full_bar(stage);
         const bool got = CG == 2
             ? warp_wait_phase_cluster(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage)
             : warp_wait_phase(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage);
