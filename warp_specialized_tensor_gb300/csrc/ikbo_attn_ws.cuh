@@ -102,10 +102,9 @@ constexpr int kAttnTmemO = kAttnSBufs * kAttnBN;
 static_assert(kAttnTmemO + kAttnDh <= 512, "TMEM columns");
 constexpr float kAttnRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kAttnRescaleBound = 256.0f;  // 2^kAttnRescaleLog2: the largest P kept
-#ifndef WST_ATTN_EARLY_TEST
-#define WST_ATTN_EARLY_TEST 40
-#endif
-constexpr int kAttnEarlyTestPair = WST_ATTN_EARLY_TEST;  // score pair of a full block at which the next S is tested
+// Score pair of a full block at which the next S product is first tested
+// (pairs 16, 32, 48 and 60 measured alike).
+constexpr int kAttnEarlyTestPair = 40;
 
 // Stream-K workspace after the 256-byte header: uint32 flags[kAttnMaxCtas][4]
 // (one per softmax warp), then one partial slot per CTA: O as [4 warps][Dh/4
