@@ -419,7 +419,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       // row, where the unshifted E[a^2] - mu^2 cancels mu^2 / var.
       // The sums are kept as packed pairs (even and odd K positions); the
       // halves are added at the end.
-      uint64_t ss2 = 0, sm2 = 0;
+      // four independent accumulator pairs (the e-th 4-byte word of each
+      // 16-byte chunk), so the adds do not form one long dependency chain
+      uint64_t ss2[4] = {0, 0, 0, 0}, sm2[4] = {0, 0, 0, 0};
       float c = 0.0f;
       uint64_t negc2 = 0;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
             for (int e = 0; e < 4; ++e) {
               const uint64_t f2 = f2_bf16x2(w[e]);
               if constexpr (NORM == 1) {
-                ss2 = f2_fma(f2, f2, ss2);
+                ss2[e] = f2_fma(f2, f2, ss2[e]);
               } else {
                 uint64_t d2 = f2_add(f2, negc2);
                 if constexpr (decltype(masked)::value) {
@@ -470,8 +472,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
                   const float dy = 8 * j + 2 * e + 1 < kvalid ? f2_hi(d2) : 0.0f;
                   asm("mov.b64 %0, {%1, %2};" : "=l"(d2) : "f"(dx), "f"(dy));
                 }
-                ss2 = f2_fma(d2, d2, ss2);
-                sm2 = f2_add(sm2, d2);
+                ss2[e] = f2_fma(d2, d2, ss2[e]);
+                sm2[e] = f2_add(sm2[e], d2);
               }
             }
           }
@@ -484,11 +486,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       }
       if (!ok) break;
       if (!warp_wait_phase(guard, scle_bar(acc), acc_phase ^ 1u, (kRoleEpilogue << 16) | 0x500 | acc)) break;
-      const float ss = f2_lo(ss2) + f2_hi(ss2);
+      const uint64_t ss_a = f2_add(f2_add(ss2[0], ss2[1]), f2_add(ss2[2], ss2[3]));
+      const float ss = f2_lo(ss_a) + f2_hi(ss_a);
       if constexpr (NORM == 1) {
         row_scale[acc * kBM + r] = rsqrtf(ss * p.inv_k + p.eps);
       } else {
-        const float sm = f2_lo(sm2) + f2_hi(sm2);
+        const uint64_t sm_a = f2_add(f2_add(sm2[0], sm2[1]), f2_add(sm2[2], sm2[3]));
+        const float sm = f2_lo(sm_a) + f2_hi(sm_a);
         // LayerNorm: mean = c + E[d], biased variance = E[d^2] - E[d]^2
         // (fp32, clamped at 0)
         const float dm = sm * p.inv_k;
