@@ -429,15 +429,16 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
         // multicast to both CTAs, arrives on consumed[s]; the peer cannot
         // wait on the leader's full[s]).  On a single CTA: the stage landed.
         const uint32_t ready = CG == 2 ? cons_bar(stage) : full_bar(stage);
-        const bool got = CG == 2
-            ? warp_wait_phase_cluster(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage)
-            : warp_wait_phase(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage);
+        // Every lane waits (and so acquires the copies' data) itself: one
+        // round of barrier latency per stage instead of lane 0's wait
+        // followed by the other lanes' acquire.
+        bool got = CG == 2 ? wait_phase_cluster(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage)
+                           : wait_phase(guard, ready, phase, (kRoleEpilogue << 16) | 0x400 | stage);
+        got = __all_sync(0xffffffffu, got);
         if (!got) {
           ok = false;
           break;
         }
-        if constexpr (CG == 2) (void)mbar_try_wait_cluster(ready, phase);  // each lane acquires the phase
-        else (void)mbar_try_wait(ready, phase);
         const uint32_t row_addr = smem_addr(smA + stage * Cfg::kABytes) + (uint32_t)r * 128u;
         if constexpr (NORM == 2) {
           if (kb == 0) {
