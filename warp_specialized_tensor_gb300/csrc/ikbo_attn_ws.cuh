@@ -581,11 +581,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int b = sb;
             // PV_{g-3} has read the P that S_g overwrites (use sph ^ 1 of
             // this buffer: the previous use completed)
-            if (nprod >= kAttnSBufs && !wait_phase(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
+            // both phases tested at once (their latencies overlap), then
+            // waited for only if not yet complete
+            const bool pv_ok = nprod < kAttnSBufs || mbar_test_wait(pv_bar(b), sph ^ 1u);
+            const bool k_ok = mbar_test_wait(kf_bar(ks), kph);
+            if (!pv_ok && !wait_phase(guard, pv_bar(b), sph ^ 1u, (kRoleMma << 16) | 0x400 | b)) {
               ok = false;
               break;
             }
-            if (!wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
+            if (!k_ok && !wait_phase(guard, kf_bar(ks), kph, (kRoleMma << 16) | ks)) { ok = false; break; }
             tc_fence_after_sync();
             const uint32_t k_addr = smem_addr(sK + ks * kAttnKBytes);
             const uint32_t d_s = tmem_base + (uint32_t)(kAttnTmemS + kAttnBN * b);
@@ -604,8 +608,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         } else {
           for (int jj = 0; jj < nb; ++jj, ++nprod) {
             const int b = sb;
-            if (!wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs) ||
-                !wait_phase(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b) ||
+            const bool v_ok = mbar_test_wait(vf_bar(vs), vph);
+            const bool p_ok = mbar_test_wait(pf_bar(b), sph);
+            if ((!v_ok && !wait_phase(guard, vf_bar(vs), vph, (kRoleMma << 16) | 0x10 | vs)) ||
+                (!p_ok && !wait_phase(guard, pf_bar(b), sph, (kRoleMma << 16) | 0x200 | b)) ||
                 (jj == 0 && !wait_phase(guard, oe_bar, (it & 1u) ^ 1u, (kRoleMma << 16) | 0x300))) {
               ok = false;
               break;
