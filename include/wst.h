@@ -92,6 +92,7 @@ typedef enum {
  * the same computation (the results are bitwise equal); the pages have no
  * counterpart.  A value applies to every later call on every thread of the
  * process; set options between calls, not while another thread is calling.
+ * (WST_OPT_NORM_STATS alone changes the order of a sum; see below.)
  *   WST_OPT_GROUPED_SCHEDULE  tile schedule of wst_grouped_gemm_bf16:
  *                             WST_SCHED_STATIC (default: persistent CTA pairs
  *                             walk the tiles in a fixed order) or
@@ -113,15 +114,34 @@ typedef enum {
  *                             16-candidate chunk launched; running CTAs take
  *                             over unstarted ones by hardware cluster launch
  *                             control).
+ *   WST_OPT_NORM_STATS        where wst_gemm_rmsnorm_bf16 and
+ *                             wst_gemm_layernorm_bf16 take the row
+ *                             statistics: WST_NORM_STATS_AUTO (default: a
+ *                             separate pass over A when N > 1024 and the
+ *                             workspace holds the statistics, else in the
+ *                             GEMM), WST_NORM_STATS_FUSED (always gathered
+ *                             in the GEMM from the A tiles in shared memory)
+ *                             or WST_NORM_STATS_PASS (always the separate
+ *                             pass; a workspace smaller than
+ *                             wst_gemm_norm_workspace_size() is then
+ *                             WST_ERR_INVALID_ARG).  The two forms sum in a
+ *                             different order: results agree to rounding,
+ *                             not bitwise.
  * wst_set_option returns WST_ERR_INVALID_ARG for an unknown option or value.
  */
 typedef enum {
   WST_OPT_GROUPED_SCHEDULE = 0,
   WST_OPT_DENSE_CTA_GROUP = 1,
-  WST_OPT_IKBO_SCHEDULE = 2
+  WST_OPT_IKBO_SCHEDULE = 2,
+  WST_OPT_NORM_STATS = 3
 } wst_option;
 
 typedef enum { WST_SCHED_STATIC = 0, WST_SCHED_CLC = 1 } wst_schedule;
+typedef enum {
+  WST_NORM_STATS_AUTO = 0,
+  WST_NORM_STATS_FUSED = 1,
+  WST_NORM_STATS_PASS = 2
+} wst_norm_stats;
 
 wst_status wst_set_option(wst_option opt, int value);
 /* Current value of an option in *value (WST_ERR_INVALID_ARG if unknown). */
@@ -160,8 +180,15 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K,
  *   r[b][m]    = 1 / sqrt( (1/K) sum_k A[b][m][k]^2 + eps )
  *   C[b][m][n] = epi( r[b][m] * sum_k A[b][m][k] * B[b][n][k] (+ bias[b][n]) )
  * i.e. y = RMSNorm(x) W^T (+ b) with the norm's learned per-feature scale
- * folded into B by the caller.  The row statistics are gathered from the A
- * tiles as they stream through shared memory, so A is read from HBM once.
+ * folded into B by the caller.  The normalised A is never formed: r is
+ * applied to the fp32 accumulators in the GEMM's epilogue.  The row
+ * statistics come either from the A tiles as they stream through shared
+ * memory (A read from HBM once; every 256-column tile of N recomputes them)
+ * or from a separate pass over A into the workspace (one more read of A,
+ * the GEMM then runs without the statistics warps); WST_OPT_NORM_STATS
+ * chooses, by default the pass when N > 1024 and workspace_bytes >=
+ * wst_gemm_norm_workspace_size(batch, M, N, strideA, strideB, 0).
+ * workspace: 16-byte aligned, at least 256 bytes (the status header).
  * Source: the TLX write-up ("How We Built TLX: A Hardware-Native GPU Compiler
  * for Production ML at Scale", companion work on norm fusion into GEMMs, and
  * "Five key areas": model-aware fusion); the pages give no formula, this is
@@ -173,7 +200,8 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
                                  const void* B, long ldb, long strideB, float eps,
                                  const void* bias, long strideBias,
                                  void* C, long ldc, long strideC, wst_dtype c_type,
-                                 wst_epilogue epi, void* workspace, void* stream);
+                                 wst_epilogue epi, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * GEMM on LayerNorm-normalised rows of A.  Same arguments, layouts and rules
@@ -185,14 +213,16 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
  * i.e. y = LayerNorm(x) W^T (+ b), the norm's per-feature scale folded into B
  * and its shift into bias by the caller.  Computed as
  *   r (A.B^T)[m][n] - r mu s[n],   r = 1/sqrt(var + eps),  s[n] = sum_k B[n][k],
- * so A is still read once: a first kernel writes the column sums s (fp32)
- * into the workspace, then the GEMM gathers sum_k A and sum_k A^2 from the A
- * tiles in shared memory (var = E[A^2] - mu^2 in fp32, clamped at 0: rows
- * whose mean is large against their spread lose precision to cancellation,
- * ~|mu|^2 / var * 2^-24 relative).
+ * a first kernel writing the column sums s (fp32) into the workspace.  The
+ * statistics are shifted-data sums in fp32 about the row's first element c
+ * (mu = c + E[d], var = E[d^2] - E[d]^2 with d = A - c, clamped at 0), taken
+ * from the A tiles in the GEMM or by a separate pass over A, as for
+ * wst_gemm_rmsnorm_bf16 (WST_OPT_NORM_STATS; the pass needs workspace_bytes
+ * >= wst_gemm_norm_workspace_size(batch, M, N, strideA, strideB, 1)).
  * workspace: 16-byte aligned, at least wst_gemm_layernorm_workspace_size(
  * batch, N, strideB) bytes (workspace_bytes says how many were given;
- * smaller returns WST_ERR_INVALID_ARG).  Two kernel launches on `stream`.
+ * smaller returns WST_ERR_INVALID_ARG).  Two or three kernel launches on
+ * `stream`.
  * Source: the same TLX norm-fusion item as wst_gemm_rmsnorm_bf16 (the pages
  * name LayerNorm and RMSNorm without formulas); standard LayerNorm reading.
  */
@@ -208,6 +238,14 @@ wst_status wst_gemm_layernorm_bf16(int batch, int M, int N, int K,
  * batch (1 when strideB == 0) rows of N fp32 column sums, each padded to a
  * multiple of 4 floats. */
 size_t wst_gemm_layernorm_workspace_size(int batch, int N, long strideB);
+
+/* Workspace bytes with which the norm GEMMs (layernorm != 0: LayerNorm) can
+ * take the row statistics from a separate pass: the header, the LayerNorm
+ * column sums, then 8 bytes (r, r*mu as two fp32) per row of A (batch * M
+ * rows; M when batch == 1 or strideA == 0), 16-byte aligned.  0 for
+ * invalid sizes. */
+size_t wst_gemm_norm_workspace_size(int batch, int M, int N, long strideA, long strideB,
+                                    int layernorm);
 
 /*
  * Grouped GEMM over G groups sharing N and K.  d_offsets is a DEVICE int32

@@ -139,6 +139,20 @@ def test_layernorm_workspace_size(lib):
     assert wst.wst_gemm_layernorm_workspace_size(0, 101, 0) == 0
 
 
+def test_norm_workspace_size(lib):
+    # header, LayerNorm column sums (padded to 4 floats, so the statistics
+    # stay 16-byte aligned), then 8 bytes of statistics per row of A
+    assert wst.wst_gemm_norm_workspace_size(1, 100, 64) == 256 + 100 * 8
+    assert wst.wst_gemm_norm_workspace_size(1, 100, 101, 0, 0, True) == 256 + 104 * 4 + 100 * 8
+    assert wst.wst_gemm_norm_workspace_size(1, 100, 100, 0, 0, True) == 256 + 100 * 4 + 100 * 8
+    # one row per batch entry when A has a batch stride, else one batch's rows
+    assert wst.wst_gemm_norm_workspace_size(3, 100, 64, 6400, 0) == 256 + 3 * 100 * 8
+    assert wst.wst_gemm_norm_workspace_size(3, 100, 64, 0, 0) == 256 + 100 * 8
+    assert wst.wst_gemm_norm_workspace_size(3, 100, 101, 6400, 4096, True) == 256 + 3 * 104 * 4 + 3 * 100 * 8
+    assert wst.wst_gemm_norm_workspace_size(0, 100, 64) == 0
+    assert wst.wst_gemm_norm_workspace_size(1, 0, 64) == 0
+
+
 def norm_gemm(fn, **kw):
     a = dict(batch=1, M=128, N=128, K=64, A=FAKE, lda=64, sA=0, B=FAKE, ldb=64, sB=0, eps=1e-5,
              bias=None, sBias=0, C=FAKE, ldc=128, sC=0, ct=1, epi=0, ws=FAKE, wsb=1 << 20, st=None)
@@ -146,9 +160,7 @@ def norm_gemm(fn, **kw):
     args = [a["batch"], a["M"], a["N"], a["K"], a["A"], a["lda"], a["sA"], a["B"], a["ldb"],
             a["sB"], a["eps"], a["bias"], a["sBias"], a["C"], a["ldc"], a["sC"], a["ct"],
             a["epi"], a["ws"]]
-    if fn.__name__ == "wst_gemm_layernorm_bf16":
-        args.append(a["wsb"])
-    return fn(*(args + [a["st"]]))
+    return fn(*(args + [a["wsb"], a["st"]]))
 
 
 @pytest.mark.parametrize("name", ["wst_gemm_rmsnorm_bf16", "wst_gemm_layernorm_bf16"])
@@ -163,6 +175,12 @@ def norm_gemm(fn, **kw):
 ])
 def test_norm_gemm_rejects(lib, name, kw, code):
     assert norm_gemm(getattr(lib, name), **kw) == code
+
+
+def test_rmsnorm_rejects_workspace_below_header(lib):
+    f = lib.wst_gemm_rmsnorm_bf16
+    assert norm_gemm(f, wsb=255) == wst.WST_ERR_INVALID_ARG
+    assert "workspace" in lib.wst_last_error().decode()
 
 
 def test_layernorm_rejects_small_workspace(lib):
@@ -207,3 +225,9 @@ def test_options_set_get_and_reject(lib):
     assert b"unknown option" in lib.wst_last_error()
     assert w.wst_get_option(w.OPT_DENSE_CTA_GROUP) == 0
     assert w.wst_get_option(w.OPT_GROUPED_SCHEDULE) == w.SCHED_STATIC
+    assert w.wst_get_option(w.OPT_NORM_STATS) == w.NORM_STATS_AUTO
+    for mode in (w.NORM_STATS_FUSED, w.NORM_STATS_PASS):
+        with w.option(w.OPT_NORM_STATS, mode):
+            assert w.wst_get_option(w.OPT_NORM_STATS) == mode
+    assert lib.wst_set_option(w.OPT_NORM_STATS, 3) == 1
+    assert w.wst_get_option(w.OPT_NORM_STATS) == w.NORM_STATS_AUTO

@@ -1,5 +1,7 @@
-"""GPU parity: GEMM on LayerNorm-normalised rows of A (row statistics fused
-into the GEMM, column sums of B from a first kernel) vs the fp64 oracle.
+"""GPU parity: GEMM on LayerNorm-normalised rows of A (the norm applied in
+the GEMM's epilogue, column sums of B from a first kernel) vs the fp64
+oracle, with the row statistics gathered in the GEMM from the A tiles and
+with them taken by a separate pass over A (every test runs under both).
 
 Tolerance: the general GEMM bound of oracle.compare applied to the
 contraction the definition states, C = x_hat . B^T with the normalised rows
@@ -26,6 +28,13 @@ def wst():
     import warp_specialized_tensor_gb300 as w
     w.load_library()
     return w
+
+
+@pytest.fixture(autouse=True, params=["fused", "pass"])
+def stats(request, wst):
+    mode = wst.NORM_STATS_FUSED if request.param == "fused" else wst.NORM_STATS_PASS
+    with wst.option(wst.OPT_NORM_STATS, mode):
+        yield request.param
 
 
 def shifted_rows(M, N, K, batch=0, seed=0, bias=False, shared_b=False, spreads=(-4.0, 4.0)):
@@ -65,7 +74,7 @@ def run(wst, d, out, eps, epi="none", B=None):
     lead = (A.shape[0],) if A.dim() == 3 else ()
     C = torch.full(lead + (A.shape[-2], B.shape[-2]), float("nan"), dtype=out, device="cuda")
     bias = d["bias"].cuda() if epi != "none" else None
-    ws = wst.layernorm_workspace(B)
+    ws = wst.norm_workspace(A, B, layernorm=True)
     wst.wst_gemm_layernorm_bf16(A, B, C, eps=eps, bias=bias, epi=epi, workspace=ws)
     assert wst.wst_sync_status(ws) == 0
     return C
@@ -116,9 +125,10 @@ def test_layernorm_padded_rows(wst):
     Bpad = torch.full((132, 128), 100.0, dtype=torch.bfloat16)
     Bpad[:, :K] = d["B"]
     Bv = Bpad.cuda()[:, :K]
+    Av = Apad.cuda()[:, :K]
     C = torch.full((200, 132), float("nan"), device="cuda")
-    ws = wst.layernorm_workspace(Bv)
-    wst.wst_gemm_layernorm_bf16(Apad.cuda()[:, :K], Bv, C, eps=1e-5, workspace=ws)
+    ws = wst.norm_workspace(Av, Bv, layernorm=True)
+    wst.wst_gemm_layernorm_bf16(Av, Bv, C, eps=1e-5, workspace=ws)
     assert wst.wst_sync_status(ws) == 0
     check(C, d, 1e-5, K)
 
@@ -155,9 +165,10 @@ def test_layernorm_matches_rmsnorm_on_centred_rows(wst):
     A[:, 64:] = -A[:, :64]
     d["A"] = A.to(torch.bfloat16)
     C_ln = run(wst, d, torch.float32, 1e-5)
-    ws = wst.workspace()
+    A, B = d["A"].cuda(), d["B"].cuda()
+    ws = wst.norm_workspace(A, B)
     C_rms = torch.empty_like(C_ln)
-    wst.wst_gemm_rmsnorm_bf16(d["A"].cuda(), d["B"].cuda(), C_rms, eps=1e-5, workspace=ws)
+    wst.wst_gemm_rmsnorm_bf16(A, B, C_rms, eps=1e-5, workspace=ws)
     assert wst.wst_sync_status(ws) == 0
     s = compare.scale(128, xhat_max(d["A"], 1e-5), amax(d["B"]))
     assert float((C_ln - C_rms).abs().max()) <= 1e-4 * s
@@ -185,3 +196,26 @@ def test_layernorm_mean_far_above_spread(wst, M, N, K, out):
     d = shifted_rows(M, N, K, seed=M + K + 7, spreads=(256.0, 288.0))
     C = run(wst, d, out, 1e-5)
     check(C, d, 1e-5, K)
+
+
+def test_layernorm_pass_needs_workspace_room(wst, stats):
+    # Column sums (one row of N floats) and then 8 bytes per row of A: the
+    # minimal LayerNorm workspace holds only the sums, so the forced pass is
+    # refused and the automatic choice keeps the statistics in the GEMM.
+    d = shifted_rows(200, 1536, 256, seed=87)
+    A, B = d["A"].cuda(), d["B"].cuda()
+    C = torch.full((200, 1536), float("nan"), device="cuda")
+    small = wst.layernorm_workspace(B)
+    assert wst.wst_gemm_norm_workspace_size(1, 200, 1536, 0, 0, True) == 256 + 1536 * 4 + 200 * 8
+    if stats == "pass":
+        with pytest.raises(wst.WstError, match="precomputed statistics"):
+            wst.wst_gemm_layernorm_bf16(A, B, C, eps=1e-5, workspace=small)
+    with wst.option(wst.OPT_NORM_STATS, wst.NORM_STATS_AUTO):
+        wst.wst_gemm_layernorm_bf16(A, B, C, eps=1e-5, workspace=small)
+        assert wst.wst_sync_status(small) == 0
+        check(C, d, 1e-5, 256)
+        C2 = torch.full_like(C, float("nan"))
+        ws = wst.norm_workspace(A, B, layernorm=True)
+        wst.wst_gemm_layernorm_bf16(A, B, C2, eps=1e-5, workspace=ws)
+        assert wst.wst_sync_status(ws) == 0
+        check(C2, d, 1e-5, 256)

@@ -1,5 +1,7 @@
-"""GPU parity: GEMM on RMS-normalised rows of A (row statistics fused into the
-GEMM) vs the fp64 oracle."""
+"""GPU parity: GEMM on RMS-normalised rows of A (the norm applied in the
+GEMM's epilogue) vs the fp64 oracle, with the row statistics gathered in the
+GEMM from the A tiles and with them taken by a separate pass over A (every
+test runs under both forms)."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +19,13 @@ def wst():
     import warp_specialized_tensor_gb300 as w
     w.load_library()
     return w
+
+
+@pytest.fixture(autouse=True, params=["fused", "pass"])
+def stats(request, wst):
+    mode = wst.NORM_STATS_FUSED if request.param == "fused" else wst.NORM_STATS_PASS
+    with wst.option(wst.OPT_NORM_STATS, mode):
+        yield request.param
 
 
 def normed_max(A, eps, rows=None):
@@ -44,7 +53,7 @@ def run(wst, d, out, eps, epi="none"):
     lead = (A.shape[0],) if A.dim() == 3 else ()
     C = torch.full(lead + (A.shape[-2], B.shape[-2]), float("nan"), dtype=out, device="cuda")
     bias = d["bias"].cuda() if epi != "none" else None
-    ws = wst.workspace()
+    ws = wst.norm_workspace(A, B)
     wst.wst_gemm_rmsnorm_bf16(A, B, C, eps=eps, bias=bias, epi=epi, workspace=ws)
     assert wst.wst_sync_status(ws) == 0
     return C
@@ -95,3 +104,26 @@ def test_rmsnorm_dense8192_sampled_rows(wst):
     C = run(wst, d, torch.bfloat16, 1e-6)
     rows = sorted(set(torch.randperm(8192, generator=torch.Generator().manual_seed(9))[:12].tolist() + [0, 8191]))
     check(C, d, 1e-6, 8192, rows=rows)
+
+
+def test_rmsnorm_pass_needs_workspace_room(wst, stats):
+    # The separate statistics pass writes 8 bytes per row of A after the
+    # header: forced, it refuses a workspace without that room; automatic,
+    # the same call falls back to the in-GEMM statistics and matches.
+    d = scaled_rows(256, 2048, 128, seed=73)
+    A, B = d["A"].cuda(), d["B"].cuda()
+    C = torch.full((256, 2048), float("nan"), device="cuda")
+    small = wst.workspace()
+    assert wst.wst_gemm_norm_workspace_size(1, 256, 2048) == 256 + 256 * 8
+    if stats == "pass":
+        with pytest.raises(wst.WstError, match="precomputed statistics"):
+            wst.wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, workspace=small)
+    with wst.option(wst.OPT_NORM_STATS, wst.NORM_STATS_AUTO):
+        wst.wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, workspace=small)     # in the GEMM
+        assert wst.wst_sync_status(small) == 0
+        check(C, d, 1e-6, 128)
+        C2 = torch.full_like(C, float("nan"))
+        ws = wst.norm_workspace(A, B)
+        wst.wst_gemm_rmsnorm_bf16(A, B, C2, eps=1e-6, workspace=ws)        # N > 1024: the pass
+        assert wst.wst_sync_status(ws) == 0
+        check(C2, d, 1e-6, 128)

@@ -22,11 +22,13 @@ __all__ = [
     "WstError", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_SILU", "EPI_BIAS_GELU", "F32", "BF16",
     "load_library", "library_path", "wst_workspace_size", "wst_workspace_init",
     "workspace", "wst_gemm_bf16", "wst_gemm_rmsnorm_bf16", "wst_gemm_layernorm_bf16",
-    "wst_gemm_layernorm_workspace_size", "layernorm_workspace", "wst_grouped_gemm_bf16",
+    "wst_gemm_layernorm_workspace_size", "layernorm_workspace", "wst_gemm_norm_workspace_size",
+    "norm_workspace", "wst_grouped_gemm_bf16",
     "wst_ikbo_linear_compress", "wst_ikbo_linear_compress_noalloc", "wst_ikbo_attention_bf16",
     "wst_ikbo_attention_workspace_size", "attention_workspace",
     "wst_sync_status", "wst_status_string", "wst_set_option", "wst_get_option", "option",
-    "OPT_GROUPED_SCHEDULE", "OPT_DENSE_CTA_GROUP", "OPT_IKBO_SCHEDULE", "SCHED_STATIC", "SCHED_CLC",
+    "OPT_GROUPED_SCHEDULE", "OPT_DENSE_CTA_GROUP", "OPT_IKBO_SCHEDULE", "OPT_NORM_STATS",
+    "SCHED_STATIC", "SCHED_CLC", "NORM_STATS_AUTO", "NORM_STATS_FUSED", "NORM_STATS_PASS",
     "wst_version", "wst_ep_dispatch_plan", "wst_ep_receive_plan", "wst_permute_rows",
 ]
 
@@ -35,8 +37,9 @@ WST_OK, WST_ERR_INVALID_ARG, WST_ERR_ALIGNMENT, WST_ERR_UNSUPPORTED = 0, 1, 2, 3
 WST_ERR_CUDA, WST_ERR_TIMEOUT, WST_ERR_BAD_OFFSETS = 4, 5, 6
 F32, BF16 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_BIAS_SILU, EPI_BIAS_GELU = 0, 1, 2, 3
-OPT_GROUPED_SCHEDULE, OPT_DENSE_CTA_GROUP, OPT_IKBO_SCHEDULE = 0, 1, 2
+OPT_GROUPED_SCHEDULE, OPT_DENSE_CTA_GROUP, OPT_IKBO_SCHEDULE, OPT_NORM_STATS = 0, 1, 2, 3
 SCHED_STATIC, SCHED_CLC = 0, 1
+NORM_STATS_AUTO, NORM_STATS_FUSED, NORM_STATS_PASS = 0, 1, 2
 _EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_silu": EPI_BIAS_SILU,
               "bias_gelu": EPI_BIAS_GELU}
 
@@ -74,13 +77,15 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wst_gemm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, P, L, P, L, L, I, I, P, P]
         lib.wst_gemm_bf16.restype = I
         lib.wst_gemm_rmsnorm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, ctypes.c_float, P, L,
-                                              P, L, L, I, I, P, P]
+                                              P, L, L, I, I, P, Z, P]
         lib.wst_gemm_rmsnorm_bf16.restype = I
         lib.wst_gemm_layernorm_bf16.argtypes = [I, I, I, I, P, L, L, P, L, L, ctypes.c_float, P,
                                                 L, P, L, L, I, I, P, Z, P]
         lib.wst_gemm_layernorm_bf16.restype = I
         lib.wst_gemm_layernorm_workspace_size.argtypes = [I, I, L]
         lib.wst_gemm_layernorm_workspace_size.restype = Z
+        lib.wst_gemm_norm_workspace_size.argtypes = [I, I, I, L, L, I]
+        lib.wst_gemm_norm_workspace_size.restype = Z
         lib.wst_grouped_gemm_bf16.argtypes = [I, I, I, I, P, L, P, L, L, P, P, L, P, L, I, I, P, P]
         lib.wst_grouped_gemm_bf16.restype = I
         lib.wst_ikbo_linear_compress.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
@@ -170,7 +175,8 @@ def _need(t, name, dtype=None, dims=None):
 def wst_set_option(opt: int, value: int) -> None:
     """Set a process-wide tuning option (OPT_GROUPED_SCHEDULE and
     OPT_IKBO_SCHEDULE: SCHED_STATIC or SCHED_CLC; OPT_DENSE_CTA_GROUP: 0
-    automatic, 1 single-CTA tiles, 2 pairs)."""
+    automatic, 1 single-CTA tiles, 2 pairs; OPT_NORM_STATS: NORM_STATS_AUTO,
+    NORM_STATS_FUSED or NORM_STATS_PASS)."""
     _check(load_library().wst_set_option(int(opt), int(value)), "wst_set_option")
 
 
@@ -282,12 +288,15 @@ def wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, bias=None, epi="none", workspace=No
                           stream=None) -> None:
     """C[b] = epi(diag(r[b]) . A[b] . B[b]^T (+ bias[b])), r = 1/sqrt(mean(A^2, -1) + eps).
 
-    Same tensor conventions as wst_gemm_bf16."""
+    Same tensor conventions as wst_gemm_bf16.  Any workspace() works; one of
+    norm_workspace(A, B) bytes also lets the row statistics come from a
+    separate pass over A (faster for wide N)."""
     batch, M, N, K, sA, sB, sC, e, sBias = _norm_gemm_args(A, B, C, bias, epi, workspace)
     st = load_library().wst_gemm_rmsnorm_bf16(
         batch, M, N, K, A.data_ptr(), A.stride(-2), sA, B.data_ptr(), B.stride(-2), sB,
         float(eps), _ptr(bias) if e else None, sBias, C.data_ptr(), C.stride(-2), sC, _ctype(C),
-        e, workspace.data_ptr(), _stream_handle(stream))
+        e, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
     _check(st, "wst_gemm_rmsnorm_bf16")
 
 
@@ -304,13 +313,33 @@ def layernorm_workspace(B, device=None, stream=None) -> torch.Tensor:
     return ws
 
 
+def wst_gemm_norm_workspace_size(batch: int, M: int, N: int, strideA: int = 0, strideB: int = 0,
+                                 layernorm: bool = False) -> int:
+    return int(load_library().wst_gemm_norm_workspace_size(batch, M, N, strideA, strideB,
+                                                           1 if layernorm else 0))
+
+
+def norm_workspace(A, B, layernorm=False, device=None, stream=None) -> torch.Tensor:
+    """A zero-filled workspace with which wst_gemm_rmsnorm_bf16 (or, with
+    layernorm=True, wst_gemm_layernorm_bf16) can take either form of the row
+    statistics for these A and B."""
+    batch = A.shape[0] if A.dim() == 3 else 1
+    n = wst_gemm_norm_workspace_size(batch, A.shape[-2], B.shape[-2], A.stride(0) if A.dim() == 3 else 0,
+                                     B.stride(0) if B.dim() == 3 else 0, layernorm)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or A.device)
+    wst_workspace_init(ws, stream)
+    return ws
+
+
 def wst_gemm_layernorm_bf16(A, B, C, eps=1e-5, bias=None, epi="none", workspace=None,
                             stream=None) -> None:
     """C[b] = epi(LayerNorm(A[b]) . B[b]^T (+ bias[b])), the rows of A normalised
     to zero mean and unit (biased) variance, eps inside the square root.
 
     Same tensor conventions as wst_gemm_bf16; the workspace must hold
-    wst_gemm_layernorm_workspace_size(...) bytes (see layernorm_workspace())."""
+    wst_gemm_layernorm_workspace_size(...) bytes (see layernorm_workspace());
+    one of norm_workspace(A, B, layernorm=True) bytes also lets the row
+    statistics come from a separate pass over A."""
     batch, M, N, K, sA, sB, sC, e, sBias = _norm_gemm_args(A, B, C, bias, epi, workspace)
     st = load_library().wst_gemm_layernorm_bf16(
         batch, M, N, K, A.data_ptr(), A.stride(-2), sA, B.data_ptr(), B.stride(-2), sB,

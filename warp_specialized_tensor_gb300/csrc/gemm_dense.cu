@@ -34,7 +34,7 @@ template <bool OUT_F32, int EPI, int CG, int NORM>
 int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream) {
   // 8 epilogue warps for SiLU / GELU (special-function heavy), except with
   // the row-statistics warps, where 4 keep the block at 384 threads.
-  constexpr int EW = (EPI >= 2 && !NORM) ? 8 : 4;
+  constexpr int EW = (EPI >= 2 && NORM != 1 && NORM != 2) ? 8 : 4;
   constexpr int kStages = stages_for<CG>();
   using Cfg = GemmCfg<kBN, kStages, EW, OUT_F32, EPI, CG, NORM>;
   auto kern = k_gemm_ws<kBN, kStages, EW, OUT_F32, EPI, CG, NORM>;
@@ -97,6 +97,8 @@ int launch_cfg(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t stream
   a.inv_k = 1.0f / (float)pr.K;
   a.colsum = pr.colsum;
   a.colsum_stride = pr.colsum_stride;
+  a.row_stats = pr.row_stats;
+  a.row_stats_stride = pr.row_stats_stride;
 
   // Persistent grid: one CTA (pair) per SM (pair) that can be resident.
   long long grid = dev.num_sms;
@@ -201,7 +203,88 @@ __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* B, long lon
   if (lane == 0) out[gw] = acc;
 }
 
+// Row statistics of A for the normalised GEMMs, one warp per row: RMSNorm
+// r = 1/sqrt(mean a^2 + eps) (shift 0); LayerNorm the shifted sums about the
+// row's first element c, mu = c + E[d], var = E[d^2] - E[d]^2, r =
+// 1/sqrt(var + eps), shift r*mu.  16-byte loads along K (rows start 16-byte
+// aligned), four in flight per lane, a scalar tail, a warp reduction.
+template <bool LN>
+__global__ void __launch_bounds__(256) k_rowstats(const __nv_bfloat16* A, long long lda,
+                                                 long long strideA, int M, int K, int rows,
+                                                 float eps, float2* out) {
+  const int gw = blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+  if (gw >= rows) return;
+  const int b = gw / M, m = gw - b * M;
+  const __nv_bfloat16* row = A + (long long)b * strideA + (long long)m * lda;
+  const float c = LN ? __bfloat162float(row[0]) : 0.0f;
+  float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const int kv = K & ~7;
+  auto add8 = [&](const uint4& w) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      const float dx = f.x - c, dy = f.y - c;
+      s2[e] = fmaf(dx, dx, fmaf(dy, dy, s2[e]));
+      if (LN) s1[e] += dx + dy;
+    }
+  };
+  int k = lane * 8;
+  for (; k + 3 * 256 < kv; k += 4 * 256) {
+    const uint4 w0 = __ldg(reinterpret_cast<const uint4*>(row + k));
+    const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(row + k + 256));
+    const uint4 w2 = __ldg(reinterpret_cast<const uint4*>(row + k + 512));
+    const uint4 w3 = __ldg(reinterpret_cast<const uint4*>(row + k + 768));
+    add8(w0);
+    add8(w1);
+    add8(w2);
+    add8(w3);
+  }
+  for (; k < kv; k += 256) add8(__ldg(reinterpret_cast<const uint4*>(row + k)));
+  for (int t = kv + lane; t < K; t += 32) {
+    const float d = __bfloat162float(row[t]) - c;
+    s2[0] = fmaf(d, d, s2[0]);
+    if (LN) s1[0] += d;
+  }
+  float ss = (s2[0] + s2[1]) + (s2[2] + s2[3]);
+  float sm = (s1[0] + s1[1]) + (s1[2] + s1[3]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (LN) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+  }
+  if (lane == 0) {
+    const float inv_k = 1.0f / (float)K;
+    if (LN) {
+      const float dm = sm * inv_k;
+      const float r = rsqrtf(fmaxf(ss * inv_k - dm * dm, 0.0f) + eps);
+      out[gw] = make_float2(r, r * (c + dm));
+    } else {
+      out[gw] = make_float2(rsqrtf(ss * inv_k + eps), 0.0f);
+    }
+  }
+}
+
 }  // namespace
+
+int run_rowstats(const void* A, long long lda, long long strideA, int nb, int M, int K, float eps,
+                 bool layernorm, float2* out, cudaStream_t stream) {
+  const long long rows = (long long)nb * M;
+  if (rows > 0x7fffffffLL) {
+    set_error("norm GEMM: %lld rows of A exceed the row-statistics kernel's range", rows);
+    return ST_UNSUPPORTED;
+  }
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(A);
+  if (layernorm)
+    k_rowstats<true><<<grid, 256, 0, stream>>>(a, lda, strideA, M, K, (int)rows, eps, out);
+  else
+    k_rowstats<false><<<grid, 256, 0, stream>>>(a, lda, strideA, M, K, (int)rows, eps, out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_rowstats");
+  return ST_OK;
+}
 
 int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
                cudaStream_t stream) {
@@ -226,6 +309,8 @@ int run_gemm(const GemmProblem& pr, cudaStream_t stream) {
   const bool pair = dense_cta_group(pr.M, pr.K) == 2;
   if (pr.norm == 1) return pair ? dispatch<2, 1>(pr, dev, stream) : dispatch<1, 1>(pr, dev, stream);
   if (pr.norm == 2) return pair ? dispatch<2, 2>(pr, dev, stream) : dispatch<1, 2>(pr, dev, stream);
+  if (pr.norm == 3) return pair ? dispatch<2, 3>(pr, dev, stream) : dispatch<1, 3>(pr, dev, stream);
+  if (pr.norm == 4) return pair ? dispatch<2, 4>(pr, dev, stream) : dispatch<1, 4>(pr, dev, stream);
   return pair ? dispatch<2, 0>(pr, dev, stream) : dispatch<1, 0>(pr, dev, stream);
 }
 

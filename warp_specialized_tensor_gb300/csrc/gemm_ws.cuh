@@ -53,6 +53,8 @@ struct GemmArgs {
   float eps, inv_k;       // row normalisation (NORM kernels only)
   const float* colsum;    // LayerNorm: s[b][n] = sum_k B[b][n][k]
   long long colsum_stride;
+  const float2* row_stats;   // NORM 3 / 4: (r, r*mu) of row m of batch b at [b * stride + m]
+  long long row_stats_stride;
 };
 
 struct Tile {
@@ -185,10 +187,13 @@ __device__ __forceinline__ void apply_norm(float (&v)[32], float scale, float sh
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-// NORM: 0 none, 1 RMSNorm, 2 LayerNorm of the rows of A.
+// NORM: 0 none, 1 RMSNorm, 2 LayerNorm of the rows of A with the row
+// statistics gathered in the kernel; 3 RMSNorm, 4 LayerNorm with them
+// precomputed (GemmArgs::row_stats).
 template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, int NORM>
 struct GemmCfg {
-  static constexpr int kStatsWarps = NORM ? 4 : 0;     // row sum-of-squares warps
+  static constexpr bool kInStats = NORM == 1 || NORM == 2;  // statistics from the ring
+  static constexpr int kStatsWarps = kInStats ? 4 : 0;     // row sum-of-squares warps
   static constexpr int kThreads = 128 + 32 * EPI_WARPS + 32 * kStatsWarps;
   static constexpr int kTileM = kBM * CG;              // rows of one (cluster) tile
   static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows
@@ -204,7 +209,7 @@ struct GemmCfg {
   static constexpr int kWarpCols = BN / (EPI_WARPS / 4);  // columns one epilogue warp drains
   static constexpr int kTmemCols = 2 * BN;
   // per-row scales (and LayerNorm shifts r*mu), 2 buffers each
-  static constexpr int kScaleBytes = NORM ? (NORM == 2 ? 4 : 2) * kBM * 4 : 0;
+  static constexpr int kScaleBytes = kInStats ? (NORM == 2 ? 4 : 2) * kBM * 4 : 0;
   static constexpr size_t kSmemBytes = (size_t)STAGES * kStageBytes +
                                        (size_t)EPI_WARPS * kStageBufs * kStgBytes + kScaleBytes +
                                        256 /*bars*/ + 1024 /*alignment slack*/;
@@ -214,8 +219,8 @@ struct GemmCfg {
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
 };
 
-// NORM: C = epi(r[m] * (A.B^T)[m][n] (+ bias)), r[m] = 1/sqrt(mean_k A[m][k]^2
-// + eps).  Four extra "stats" warps read every A stage from the ring (each
+// NORM 1 / 2: C = epi(r[m] * (A.B^T)[m][n] (+ bias)), r[m] = 1/sqrt(mean_k
+// A[m][k]^2 + eps) (LayerNorm: minus r[m] mu[m] s[n]).  Four extra "stats" warps read every A stage from the ring (each
 // lane one row: eight 16-byte swizzled chunks per stage), accumulate the
 // row's sum of squares in fp32, release the stage together with the MMA, and
 // hand 1/sqrt(ss/K + eps) per row to the epilogue through a double-buffered
@@ -228,7 +233,10 @@ struct GemmCfg {
 // they have read the stage.  (In a pair, both CTAs' loads complete on the
 // leader's full[s], which the peer's warps cannot wait on; relaying full[s]
 // to the peer with a thread's remote arrive per stage ran 2.6x slower on
-// GB300.)
+// GB300.)  Every tile recomputes its rows' statistics, so across the N tiles
+// of a row band the work repeats N / BN times; NORM 3 / 4 instead read r and
+// r*mu per row from a buffer a separate pass over A filled (no stats warps,
+// the plain GEMM's ring), which is faster once N spans several tiles.
 //
 // CG = 2: a cluster of two CTAs computes one 256 x BN tile with
 // tcgen05.mma.cta_group::2 issued by the even CTA (the leader).  Each CTA
@@ -237,7 +245,7 @@ struct GemmCfg {
 // arrive on empty[s] / acc_full[a] in both CTAs; both epilogues arrive on the
 // leader's acc_empty[a]; each CTA drains its own 128 accumulator rows.
 template <int BN, int STAGES, int EPI_WARPS, bool OUT_F32, int EPI, int CG, int NORM>
-__global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
+__global__ void __launch_bounds__(128 + 32 * EPI_WARPS + ((NORM == 1 || NORM == 2) ? 128 : 0), 1)
     k_gemm_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
   using Cfg = GemmCfg<BN, STAGES, EPI_WARPS, OUT_F32, EPI, CG, NORM>;
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       // by the stats warps, which wait for the MMA commit on consumed[s],
       // and on single CTAs by both (the stats warps read the stage as soon
       // as it lands, alongside the MMAs)
-      mbar_init(empty_bar(s), !NORM ? 1 : (CG == 1 ? 1 + Cfg::kStatsWarps : Cfg::kStatsWarps));
+      mbar_init(empty_bar(s), !Cfg::kInStats ? 1 : (CG == 1 ? 1 + Cfg::kStatsWarps : Cfg::kStatsWarps));
       mbar_init(cons_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
           // slot free (in both CTAs) once these MMAs finish; with the row
           // statistics, once the stats warps have read it too (on a pair,
           // after these MMAs)
-          const uint32_t rel = (NORM && CG == 2) ? cons_bar(stage) : empty_bar(stage);
+          const uint32_t rel = (Cfg::kInStats && CG == 2) ? cons_bar(stage) : empty_bar(stage);
           if constexpr (CG == 1) umma_commit(rel);
           else                   umma_commit_pair(rel, 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -401,7 +409,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
     }
-  } else if (NORM && warp >= 4 + EPI_WARPS) {
+  } else if (Cfg::kInStats && warp >= 4 + EPI_WARPS) {
     // ------------------------------------------------------------------ row statistics
     const int r = (warp - 4 - EPI_WARPS) * 32 + (int)lane;  // CTA-local row of A
     int stage = 0;
@@ -529,10 +537,17 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       const bool full_rows = row_base + 32 <= tl.row_end;
       const __nv_bfloat16* bias_row =
           EPI ? p.bias + (long long)tl.b * p.bias_stride : nullptr;
-      const float* cs_row = NORM == 2 ? p.colsum + (long long)tl.b * p.colsum_stride : nullptr;
+      const float* cs_row = (NORM == 2 || NORM == 4) ? p.colsum + (long long)tl.b * p.colsum_stride : nullptr;
       const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       float scale = 1.0f, shift = 0.0f;
-      if constexpr (NORM) {
+      if constexpr (NORM >= 3) {
+        // precomputed statistics of this lane's row
+        if (row < tl.row_end) {
+          const float2 rs = __ldg(p.row_stats + (long long)tl.b * p.row_stats_stride + row);
+          scale = rs.x;
+          shift = rs.y;
+        }
+      } else if constexpr (NORM) {
         if (!warp_wait_phase(guard, sclf_bar(acc), acc_phase, (kRoleEpilogue << 16) | 0x600 | acc)) break;
         (void)mbar_try_wait(sclf_bar(acc), acc_phase);
         scale = row_scale[acc * kBM + q * 32 + (int)lane];
@@ -545,13 +560,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS + (NORM ? 128 : 0), 1)
       for (int c0 = col_begin; c0 < col_begin + Cfg::kWarpCols; c0 += Cfg::kColsPerChunk) {
         float v0[32];
         tmem_load32(t_lane + c0, v0);
-        if constexpr (NORM) apply_norm<NORM>(v0, scale, shift, cs_row, tl.n0 + c0, p.N);
+        if constexpr (NORM) apply_norm<(NORM == 2 || NORM == 4) ? 2 : 1>(v0, scale, shift, cs_row, tl.n0 + c0, p.N);
         apply_bias_act<EPI>(v0, bias_row, tl.n0 + c0, p.N);
         uint32_t packed[16];
         float v1[32];
         if constexpr (!OUT_F32) {
           tmem_load32(t_lane + c0 + 32, v1);
-          if constexpr (NORM) apply_norm<NORM>(v1, scale, shift, cs_row, tl.n0 + c0 + 32, p.N);
+          if constexpr (NORM) apply_norm<(NORM == 2 || NORM == 4) ? 2 : 1>(v1, scale, shift, cs_row, tl.n0 + c0 + 32, p.N);
           apply_bias_act<EPI>(v1, bias_row, tl.n0 + c0 + 32, p.N);
 #pragma unroll
           for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);

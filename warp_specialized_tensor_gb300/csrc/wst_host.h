@@ -33,7 +33,13 @@ struct DeviceInfo {
 int current_device_info(DeviceInfo* out);  // Status
 
 // Process-wide tuning options (wst_option in include/wst.h).
-enum Option : int { OPT_GROUPED_SCHEDULE = 0, OPT_DENSE_CTA_GROUP = 1, OPT_IKBO_SCHEDULE = 2, OPT_COUNT = 3 };
+enum Option : int {
+  OPT_GROUPED_SCHEDULE = 0,
+  OPT_DENSE_CTA_GROUP = 1,
+  OPT_IKBO_SCHEDULE = 2,
+  OPT_NORM_STATS = 3,
+  OPT_COUNT = 4
+};
 int option_value(int opt);
 
 unsigned long long wait_timeout_ns();
@@ -80,6 +86,8 @@ struct GemmProblem {
   float eps;
   const float* colsum;        // LayerNorm: column sums of B, [batch][N] (stride 0: shared)
   long long colsum_stride;
+  const float2* row_stats;    // norm 3 / 4: precomputed (r, r*mu) per row of A
+  long long row_stats_stride;
 };
 
 struct IkboProblem {
@@ -109,6 +117,8 @@ struct AttnProblem {
 
 int run_gemm(const GemmProblem& p, cudaStream_t stream);
 // s[b][n] = sum_k B[b][n][k] in fp32 for b < nb (LayerNorm fusion).
+int run_rowstats(const void* A, long long lda, long long strideA, int nb, int M, int K, float eps,
+                 bool layernorm, float2* out, cudaStream_t stream);
 int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
                cudaStream_t stream);
 int run_ikbo_attention(const AttnProblem& p, cudaStream_t stream);
