@@ -133,6 +133,23 @@ def test_layernorm_padded_rows(wst):
     check(C, d, 1e-5, K)
 
 
+def test_layernorm_batched_b_ragged_n(wst):
+    # A batch stride on B and N = 101, not a multiple of 4: each batch
+    # entry's column sums start on a padded row of 104 floats (the epilogue
+    # reads them as float4), so entries past the first must land there.
+    # C is a view with a padded row (ldc = 104) to meet the 16-byte rule.
+    M, N, K = 200, 101, 256
+    d = shifted_rows(M, N, K, batch=3, seed=88)
+    A, B = d["A"].cuda(), d["B"].cuda()
+    Cfull = torch.full((3, M, 104), float("nan"), device="cuda")
+    C = Cfull[..., :N]
+    ws = wst.norm_workspace(A, B, layernorm=True)
+    wst.wst_gemm_layernorm_bf16(A, B, C, eps=1e-5, workspace=ws)
+    assert wst.wst_sync_status(ws) == 0
+    check(C, d, 1e-5, K)
+    assert torch.isnan(Cfull[..., N:]).all()   # the padding is never written
+
+
 def test_layernorm_constant_rows(wst):
     # A constant row has zero variance: its normalised row is 0 and C is the
     # bias alone (the epilogue applied to it).

@@ -176,128 +176,148 @@ int run_gemm_grouped(const GemmProblem& pr, const DeviceInfo& dev, cudaStream_t 
 
 namespace {
 
-// One warp per row of B: 16-byte vector loads along K (rows start 16-byte
-// aligned: B and its strides are), a scalar tail, then a warp reduction.
-__global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* B, long long ldb,
-                                               long long strideB, int N, int K, int rows,
-                                               float* out) {
-  const int gw = blockIdx.x * 8 + (int)(threadIdx.x >> 5);
-  const int lane = (int)(threadIdx.x & 31);
-  if (gw >= rows) return;
-  const int b = gw / N, n = gw - b * N;
-  const __nv_bfloat16* row = B + (long long)b * strideB + (long long)n * ldb;
-  float acc = 0.0f;
+// The passes over rows of bf16 data ahead of the norm GEMMs, in one launch
+// and one warp per row: the row statistics of A (the first ceil(rows_a / 8)
+// blocks) and the column sums s[n] = sum_k B[n][k] of B (the rest).
+// Statistics: RMSNorm r = 1/sqrt(mean a^2 + eps), shift 0; LayerNorm the
+// sums of d = a - c and d^2 about the row's first element c, mu = c + E[d],
+// var = E[d^2] - E[d]^2 (clamped at 0), r = 1/sqrt(var + eps), shift r*mu,
+// the same formulas as the GEMM's statistics warps.  Rows start 16-byte
+// aligned (the operands and their strides are); each lane keeps eight
+// 16-byte loads in flight (a row of 8192 bf16 is four rounds), then a
+// scalar tail and a warp reduction.
+struct NormPassArgs {
+  const __nv_bfloat16* A;
+  long long lda, strideA;
+  int M, K, rows_a;
+  float eps;
+  float2* stats;
+  const __nv_bfloat16* B;
+  long long ldb, strideB;
+  int N, rows_b;
+  long long colsum_stride;
+  float* colsum;
+};
+
+// Calls f(w) for every 16-byte chunk of the row's first K & ~7 elements
+// that falls to this lane, eight loads at a time, and returns where the
+// scalar tail starts.
+template <class F>
+__device__ __forceinline__ int sweep_row(const __nv_bfloat16* row, int K, int lane, F&& f) {
   const int kv = K & ~7;
-  for (int k = lane * 8; k < kv; k += 256) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + k));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+  int k = lane * 8;
+  for (; k + 7 * 256 < kv; k += 8 * 256) {
+    uint4 w[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      acc += f.x + f.y;
-    }
+    for (int u = 0; u < 8; ++u) w[u] = __ldg(reinterpret_cast<const uint4*>(row + k + u * 256));
+#pragma unroll
+    for (int u = 0; u < 8; ++u) f(w[u]);
   }
-  for (int k = kv + lane; k < K; k += 32) acc += __bfloat162float(row[k]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) out[gw] = acc;
+  for (; k < kv; k += 256) f(__ldg(reinterpret_cast<const uint4*>(row + k)));
+  return kv;
 }
 
-// Row statistics of A for the normalised GEMMs, one warp per row: RMSNorm
-// r = 1/sqrt(mean a^2 + eps) (shift 0); LayerNorm the shifted sums about the
-// row's first element c, mu = c + E[d], var = E[d^2] - E[d]^2, r =
-// 1/sqrt(var + eps), shift r*mu.  16-byte loads along K (rows start 16-byte
-// aligned), four in flight per lane, a scalar tail, a warp reduction.
 template <bool LN>
-__global__ void __launch_bounds__(256) k_rowstats(const __nv_bfloat16* A, long long lda,
-                                                 long long strideA, int M, int K, int rows,
-                                                 float eps, float2* out) {
-  const int gw = blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+__global__ void __launch_bounds__(256) k_norm_pass(const NormPassArgs a) {
   const int lane = (int)(threadIdx.x & 31);
-  if (gw >= rows) return;
-  const int b = gw / M, m = gw - b * M;
-  const __nv_bfloat16* row = A + (long long)b * strideA + (long long)m * lda;
-  const float c = LN ? __bfloat162float(row[0]) : 0.0f;
-  float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const int kv = K & ~7;
-  auto add8 = [&](const uint4& w) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+  const int blocks_a = (a.rows_a + 7) / 8;
+  if ((int)blockIdx.x < blocks_a) {
+    const int gw = (int)blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+    if (gw >= a.rows_a) return;
+    const int b = gw / a.M, m = gw - b * a.M;
+    const __nv_bfloat16* row = a.A + (long long)b * a.strideA + (long long)m * a.lda;
+    const float c = LN ? __bfloat162float(row[0]) : 0.0f;
+    float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int kv = sweep_row(row, a.K, lane, [&](const uint4& w) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      const float dx = f.x - c, dy = f.y - c;
-      s2[e] = fmaf(dx, dx, fmaf(dy, dy, s2[e]));
-      if (LN) s1[e] += dx + dy;
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        const float dx = f.x - c, dy = f.y - c;
+        s2[e] = fmaf(dx, dx, fmaf(dy, dy, s2[e]));
+        if (LN) s1[e] += dx + dy;
+      }
+    });
+    for (int t = kv + lane; t < a.K; t += 32) {
+      const float d = __bfloat162float(row[t]) - c;
+      s2[0] = fmaf(d, d, s2[0]);
+      if (LN) s1[0] += d;
     }
-  };
-  int k = lane * 8;
-  for (; k + 3 * 256 < kv; k += 4 * 256) {
-    const uint4 w0 = __ldg(reinterpret_cast<const uint4*>(row + k));
-    const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(row + k + 256));
-    const uint4 w2 = __ldg(reinterpret_cast<const uint4*>(row + k + 512));
-    const uint4 w3 = __ldg(reinterpret_cast<const uint4*>(row + k + 768));
-    add8(w0);
-    add8(w1);
-    add8(w2);
-    add8(w3);
-  }
-  for (; k < kv; k += 256) add8(__ldg(reinterpret_cast<const uint4*>(row + k)));
-  for (int t = kv + lane; t < K; t += 32) {
-    const float d = __bfloat162float(row[t]) - c;
-    s2[0] = fmaf(d, d, s2[0]);
-    if (LN) s1[0] += d;
-  }
-  float ss = (s2[0] + s2[1]) + (s2[2] + s2[3]);
-  float sm = (s1[0] + s1[1]) + (s1[2] + s1[3]);
+    float ss = (s2[0] + s2[1]) + (s2[2] + s2[3]);
+    float sm = (s1[0] + s1[1]) + (s1[2] + s1[3]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (LN) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-  }
-  if (lane == 0) {
-    const float inv_k = 1.0f / (float)K;
-    if (LN) {
-      const float dm = sm * inv_k;
-      const float r = rsqrtf(fmaxf(ss * inv_k - dm * dm, 0.0f) + eps);
-      out[gw] = make_float2(r, r * (c + dm));
-    } else {
-      out[gw] = make_float2(rsqrtf(ss * inv_k + eps), 0.0f);
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (LN) sm += __shfl_xor_sync(0xffffffffu, sm, o);
     }
+    if (lane == 0) {
+      const float inv_k = 1.0f / (float)a.K;
+      if (LN) {
+        const float dm = sm * inv_k;
+        const float r = rsqrtf(fmaxf(ss * inv_k - dm * dm, 0.0f) + a.eps);
+        a.stats[gw] = make_float2(r, r * (c + dm));
+      } else {
+        a.stats[gw] = make_float2(rsqrtf(ss * inv_k + a.eps), 0.0f);
+      }
+    }
+  } else {
+    const int gw = ((int)blockIdx.x - blocks_a) * 8 + (int)(threadIdx.x >> 5);
+    if (gw >= a.rows_b) return;
+    const int b = gw / a.N, n = gw - b * a.N;
+    const __nv_bfloat16* row = a.B + (long long)b * a.strideB + (long long)n * a.ldb;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int kv = sweep_row(row, a.K, lane, [&](const uint4& w) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        acc[e] += f.x + f.y;
+      }
+    });
+    for (int t = kv + lane; t < a.K; t += 32) acc[0] += __bfloat162float(row[t]);
+    float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    // each batch entry's sums start on a padded row (the epilogue reads
+    // them as float4)
+    if (lane == 0) a.colsum[(long long)b * a.colsum_stride + n] = sum;
   }
 }
 
 }  // namespace
 
-int run_rowstats(const void* A, long long lda, long long strideA, int nb, int M, int K, float eps,
-                 bool layernorm, float2* out, cudaStream_t stream) {
-  const long long rows = (long long)nb * M;
-  if (rows > 0x7fffffffLL) {
-    set_error("norm GEMM: %lld rows of A exceed the row-statistics kernel's range", rows);
+int run_norm_pass(const NormPass& np, cudaStream_t stream) {
+  const long long rows_a = np.stats ? (long long)np.nb_a * np.M : 0;
+  const long long rows_b = np.colsum ? (long long)np.nb_b * np.N : 0;
+  if (rows_a > 0x7fffffffLL || rows_b > 0x7fffffffLL) {
+    set_error("norm GEMM: %lld rows of A / %lld rows of B exceed the statistics kernel's range",
+              rows_a, rows_b);
     return ST_UNSUPPORTED;
   }
-  const unsigned grid = (unsigned)((rows + 7) / 8);
-  const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(A);
-  if (layernorm)
-    k_rowstats<true><<<grid, 256, 0, stream>>>(a, lda, strideA, M, K, (int)rows, eps, out);
+  if (rows_a + rows_b == 0) return ST_OK;
+  NormPassArgs a{};
+  a.A = static_cast<const __nv_bfloat16*>(np.A);
+  a.lda = np.lda;
+  a.strideA = np.strideA;
+  a.M = np.M;
+  a.K = np.K;
+  a.rows_a = (int)rows_a;
+  a.eps = np.eps;
+  a.stats = np.stats;
+  a.B = static_cast<const __nv_bfloat16*>(np.B);
+  a.ldb = np.ldb;
+  a.strideB = np.strideB;
+  a.N = np.N;
+  a.rows_b = (int)rows_b;
+  a.colsum_stride = np.colsum_stride;
+  a.colsum = np.colsum;
+  const unsigned grid = (unsigned)((rows_a + 7) / 8 + (rows_b + 7) / 8);
+  if (np.layernorm)
+    k_norm_pass<true><<<grid, 256, 0, stream>>>(a);
   else
-    k_rowstats<false><<<grid, 256, 0, stream>>>(a, lda, strideA, M, K, (int)rows, eps, out);
+    k_norm_pass<false><<<grid, 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "launch k_rowstats");
-  return ST_OK;
-}
-
-int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
-               cudaStream_t stream) {
-  const long long rows = (long long)nb * N;
-  if (rows > 0x7fffffffLL) {
-    set_error("layernorm: %lld rows of B exceed the column-sum kernel's range", rows);
-    return ST_UNSUPPORTED;
-  }
-  const unsigned grid = (unsigned)((rows + 7) / 8);
-  k_colsum<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(B), ldb, strideB, N, K,
-                                     (int)rows, s);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "launch k_colsum");
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_norm_pass");
   return ST_OK;
 }
 

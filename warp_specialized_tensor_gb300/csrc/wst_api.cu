@@ -377,17 +377,24 @@ int choose_prestats(const GemmProblem& p, bool layernorm, size_t workspace_bytes
   return WST_OK;
 }
 
-int run_prestats(GemmProblem& p, bool layernorm, cudaStream_t st) {
+// Adds the statistics of A to the pass and points the GEMM (NORM 3 / 4) at
+// them: one batch's rows when A is shared by the batch.
+void plan_prestats(GemmProblem& p, bool layernorm, NormPass& np) {
   const bool shared_a = !(p.batch > 1 && p.strideA != 0);
   float2* out = reinterpret_cast<float2*>(static_cast<uint8_t*>(p.ws) +
                                           stats_offset(p.batch, p.N, p.strideB, layernorm));
-  const int rc = run_rowstats(p.A, p.lda, shared_a ? 0 : p.strideA, shared_a ? 1 : p.batch, p.M,
-                              p.K, p.eps, layernorm, out, st);
-  if (rc) return rc;
+  np.A = p.A;
+  np.lda = p.lda;
+  np.strideA = shared_a ? 0 : p.strideA;
+  np.nb_a = shared_a ? 1 : p.batch;
+  np.M = p.M;
+  np.K = p.K;
+  np.eps = p.eps;
+  np.layernorm = layernorm;
+  np.stats = out;
   p.row_stats = out;
   p.row_stats_stride = shared_a ? 0 : p.M;
   p.norm = layernorm ? 4 : 3;
-  return WST_OK;
 }
 
 }  // namespace
@@ -414,7 +421,11 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K, const void* A, 
   WST_TRY((wst_status)choose_prestats(p, false, workspace_bytes, pre));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   p.norm = 1;
-  if (pre) WST_TRY((wst_status)run_prestats(p, false, st));
+  if (pre) {
+    NormPass np{};
+    plan_prestats(p, false, np);
+    WST_TRY((wst_status)run_norm_pass(np, st));
+  }
   return (wst_status)run_gemm(p, st);
 }
 
@@ -440,9 +451,21 @@ wst_status wst_gemm_layernorm_bf16(int batch, int M, int N, int K, const void* A
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   bool pre = false;
   WST_TRY((wst_status)choose_prestats(p, true, workspace_bytes, pre));
-  WST_TRY((wst_status)run_colsum(B, ldb, nb > 1 ? strideB : 0, nb, N, K, s, st));
+  // the column sums of B, and with the separate pass the statistics of A,
+  // in one launch
+  NormPass np{};
+  np.B = B;
+  np.ldb = ldb;
+  np.strideB = nb > 1 ? strideB : 0;
+  np.nb_b = nb;
+  np.N = N;
+  np.K = K;
+  np.layernorm = true;
+  np.colsum_stride = colsum_stride(N);
+  np.colsum = s;
   p.norm = 2;
-  if (pre) WST_TRY((wst_status)run_prestats(p, true, st));
+  if (pre) plan_prestats(p, true, np);
+  WST_TRY((wst_status)run_norm_pass(np, st));
   p.colsum = s;
   p.colsum_stride = nb > 1 ? colsum_stride(N) : 0;
   return (wst_status)run_gemm(p, st);

@@ -117,10 +117,24 @@ struct AttnProblem {
 
 int run_gemm(const GemmProblem& p, cudaStream_t stream);
 // s[b][n] = sum_k B[b][n][k] in fp32 for b < nb (LayerNorm fusion).
-int run_rowstats(const void* A, long long lda, long long strideA, int nb, int M, int K, float eps,
-                 bool layernorm, float2* out, cudaStream_t stream);
-int run_colsum(const void* B, long long ldb, long long strideB, int nb, int N, int K, float* s,
-               cudaStream_t stream);
+// Passes over rows of bf16 data ahead of the norm GEMMs, one launch: the
+// row statistics (r, r*mu) of nb_a x M rows of A into stats (none when stats
+// is NULL) and the column sums of nb_b x N rows of B into colsum, batch entry
+// b's row starting at b * colsum_stride floats (none when colsum is NULL).
+struct NormPass {
+  const void* A;
+  long long lda, strideA;
+  int nb_a, M, K;
+  float eps;
+  bool layernorm;
+  float2* stats;
+  const void* B;
+  long long ldb, strideB;
+  int nb_b, N;
+  long long colsum_stride;
+  float* colsum;
+};
+int run_norm_pass(const NormPass& np, cudaStream_t stream);
 int run_ikbo_attention(const AttnProblem& p, cudaStream_t stream);
 size_t attention_workspace_bytes();
 int run_ikbo(const IkboProblem& p, cudaStream_t stream);
