@@ -127,3 +127,35 @@ def test_rmsnorm_pass_needs_workspace_room(wst, stats):
         wst.wst_gemm_rmsnorm_bf16(A, B, C2, eps=1e-6, workspace=ws)        # N > 1024: the pass
         assert wst.wst_sync_status(ws) == 0
         check(C2, d, 1e-6, 128)
+
+
+@pytest.mark.parametrize("layernorm", [False, True])
+def test_norm_shared_a_batched_b_through_abi(wst, stats, layernorm):
+    # batch = 3 with strideA = 0 (one A shared by the batch) and a batched B,
+    # through the C ABI (the Python binding takes the batch from A): the
+    # separate pass then computes one batch's row statistics and every batch
+    # entry's epilogue reads them.
+    M, N, K, batch = 200, 256, 320, 3
+    d = scaled_rows(M, N, K, seed=74)
+    Bb = synthetic.dense(M, N, K, batch=batch, seed=75)["B"]
+    A, B = d["A"].cuda(), Bb.cuda()
+    C = torch.full((batch, M, N), float("nan"), device="cuda")
+    nbytes = wst.wst_gemm_norm_workspace_size(batch, M, N, 0, B.stride(0), layernorm)
+    assert nbytes == 256 + (batch * N * 4 if layernorm else 0) + M * 8
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    lib = wst.load_library()
+    fn = lib.wst_gemm_layernorm_bf16 if layernorm else lib.wst_gemm_rmsnorm_bf16
+    st = fn(batch, M, N, K, A.data_ptr(), K, 0, B.data_ptr(), K, B.stride(0), 1e-5, None, 0,
+            C.data_ptr(), N, M * N, wst.F32, wst.EPI_NONE, ws.data_ptr(), nbytes, None)
+    assert st == 0, lib.wst_last_error()
+    assert wst.wst_sync_status(ws) == 0
+    A3 = d["A"].expand(batch, M, K).contiguous()
+    ref = (oracle.gemm_layernorm if layernorm else oracle.gemm_rmsnorm)(A3, Bb, eps=1e-5)
+    a = A3.float().numpy().astype(np.float64)
+    if layernorm:
+        mu = a.mean(axis=-1, keepdims=True)
+        amax_n = float((np.abs(a - mu) / np.sqrt(((a - mu) ** 2).mean(axis=-1, keepdims=True) + 1e-5)).max())
+    else:
+        amax_n = normed_max(A3, 1e-5)
+    ok, metric, detail = compare.check(C.cpu().numpy(), ref, K, amax_n, amax(Bb), False)
+    assert ok, detail
