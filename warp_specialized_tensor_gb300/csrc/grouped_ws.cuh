@@ -79,9 +79,13 @@ constexpr int kGrpThinMaxRows = 64;            // per CTA
 constexpr int kGrpStageBytes = kGrpWBytes + kGrpXBytes;
 constexpr int kGrpStgBytes = 32 * 32 * 4;      // per-warp transpose buffer (fp32 worst case)
 constexpr int kGrpStgBufs = 2;                 // double-buffered for the TMA stores
+// Group offsets copied to shared memory at the start (problems of up to
+// kGrpTabMax - 1 groups): walking the groups there instead of through
+// dependent global loads keeps the tile boundaries short.
+constexpr int kGrpTabMax = 256;
 constexpr size_t kGrpSmemBytes = (size_t)kGrpStages * kGrpStageBytes +
                                  (size_t)kGrpEpiWarps * kGrpStgBufs * kGrpStgBytes +
-                                 512 /*barriers, queue*/ + 1024;
+                                 512 /*barriers, queue*/ + kGrpTabMax * 4 + 1024;
 static_assert(kGrpSmemBytes <= 232448, "shared memory per CTA");
 
 struct GroupedArgs {
@@ -111,11 +115,12 @@ struct GrpWalker {
   int g;
   long long base, count;
   int r0, r1, tt, sz;  // rows, token tiles, token-tile width
+  const int* tab;      // the offsets in shared memory, or nullptr
 
   __device__ __forceinline__ void load(const GroupedArgs& p) {
     if (g >= p.G) { count = 0; return; }
-    int a = __ldg(p.offsets + g);
-    int b = __ldg(p.offsets + g + 1);
+    int a = tab ? tab[g] : __ldg(p.offsets + g);
+    int b = tab ? tab[g + 1] : __ldg(p.offsets + g + 1);
     a = min(max(a, 0), p.M_total);
     b = min(max(b, a), p.M_total);
     r0 = a;
@@ -124,11 +129,13 @@ struct GrpWalker {
     sz = kGrpTileT;
     count = (long long)tt * p.n_tiles;
   }
-  __device__ __forceinline__ void init(const GroupedArgs& p) {
+  __device__ __forceinline__ void init(const GroupedArgs& p, const int* table) {
+    tab = table;
     g = 0;
     base = 0;
     load(p);
   }
+  __device__ __forceinline__ void init(const GroupedArgs& p) { init(p, tab); }
   __device__ __forceinline__ bool seek(const GroupedArgs& p, long long t) {
     if (t < base) init(p);
     while (g < p.G && t >= base + count) {
@@ -214,6 +221,8 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile int* tq_id = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [kGrpTQ]
   static_assert(kNumBars * 8 + 16 + (2 + kGrpTQ) * 4 <= 512, "barrier area");
+  int* off_tab = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 512);
+  const int* tab = p.G < kGrpTabMax ? off_tab : nullptr;
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
@@ -268,6 +277,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     tmem_alloc<2>(smem_addr(tmem_slot), 512);
     tmem_relinquish<2>();
   }
+  if (warp == 3 && tab) {
+    for (int i = (int)lane; i <= p.G; i += 32) off_tab[i] = min(max(__ldg(p.offsets + i), 0), p.M_total);
+  }
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();
@@ -301,7 +313,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       GrpWalker gw;
-      gw.init(p);
+      gw.init(p, tab);
       int tqs = 0;
       uint32_t tqph = 0;
       long long t = 0;
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       GrpWalker gw;
-      gw.init(p);
+      gw.init(p, tab);
       int tqs = 0;
       uint32_t tqph = 0;
       long long t = 0;
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           return true;
         };
         GrpWalker sw;
-        sw.init(p);
+        sw.init(p, tab);
         bool ok = push((int)cluster_id);
         while (ok) {
           if (rank == 0) {
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     GrpWalker gw;
-    gw.init(p);
+    gw.init(p, tab);
     int tqs = 0;
     uint32_t tqph = 0;
     long long t = 0;
