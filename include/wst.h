@@ -117,9 +117,9 @@ typedef enum {
  *   WST_OPT_NORM_STATS        where wst_gemm_rmsnorm_bf16 and
  *                             wst_gemm_layernorm_bf16 take the row
  *                             statistics: WST_NORM_STATS_AUTO (default: a
- *                             separate pass over A when N > 1024 and the
- *                             workspace holds the statistics, else in the
- *                             GEMM), WST_NORM_STATS_FUSED (always gathered
+ *                             separate pass over A when N > 2048 (RMSNorm)
+ *                             or N > 512 (LayerNorm) and the workspace
+ *                             holds the statistics, else in the GEMM), WST_NORM_STATS_FUSED (always gathered
  *                             in the GEMM from the A tiles in shared memory)
  *                             or WST_NORM_STATS_PASS (always the separate
  *                             pass; a workspace smaller than
@@ -186,7 +186,7 @@ wst_status wst_gemm_bf16(int batch, int M, int N, int K,
  * memory (A read from HBM once; every 256-column tile of N recomputes them)
  * or from a separate pass over A into the workspace (one more read of A,
  * the GEMM then runs without the statistics warps); WST_OPT_NORM_STATS
- * chooses, by default the pass when N > 1024 and workspace_bytes >=
+ * chooses, by default the pass when N > 2048 and workspace_bytes >=
  * wst_gemm_norm_workspace_size(batch, M, N, strideA, strideB, 0).
  * workspace: 16-byte aligned, at least 256 bytes (the status header).
  * Source: the TLX write-up ("How We Built TLX: A Hardware-Native GPU Compiler
@@ -217,8 +217,9 @@ wst_status wst_gemm_rmsnorm_bf16(int batch, int M, int N, int K,
  * statistics are shifted-data sums in fp32 about the row's first element c
  * (mu = c + E[d], var = E[d^2] - E[d]^2 with d = A - c, clamped at 0), taken
  * from the A tiles in the GEMM or by a separate pass over A, as for
- * wst_gemm_rmsnorm_bf16 (WST_OPT_NORM_STATS; the pass needs workspace_bytes
- * >= wst_gemm_norm_workspace_size(batch, M, N, strideA, strideB, 1)).
+ * wst_gemm_rmsnorm_bf16 (WST_OPT_NORM_STATS; by default the pass when N >
+ * 512 and workspace_bytes >= wst_gemm_norm_workspace_size(batch, M, N,
+ * strideA, strideB, 1)).
  * workspace: 16-byte aligned, at least wst_gemm_layernorm_workspace_size(
  * batch, N, strideB) bytes (workspace_bytes says how many were given;
  * smaller returns WST_ERR_INVALID_ARG).  Two or three kernel launches on

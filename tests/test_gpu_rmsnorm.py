@@ -110,11 +110,11 @@ def test_rmsnorm_pass_needs_workspace_room(wst, stats):
     # The separate statistics pass writes 8 bytes per row of A after the
     # header: forced, it refuses a workspace without that room; automatic,
     # the same call falls back to the in-GEMM statistics and matches.
-    d = scaled_rows(256, 2048, 128, seed=73)
+    d = scaled_rows(256, 4096, 128, seed=73)
     A, B = d["A"].cuda(), d["B"].cuda()
-    C = torch.full((256, 2048), float("nan"), device="cuda")
+    C = torch.full((256, 4096), float("nan"), device="cuda")
     small = wst.workspace()
-    assert wst.wst_gemm_norm_workspace_size(1, 256, 2048) == 256 + 256 * 8
+    assert wst.wst_gemm_norm_workspace_size(1, 256, 4096) == 256 + 256 * 8
     if stats == "pass":
         with pytest.raises(wst.WstError, match="precomputed statistics"):
             wst.wst_gemm_rmsnorm_bf16(A, B, C, eps=1e-6, workspace=small)
@@ -124,7 +124,7 @@ def test_rmsnorm_pass_needs_workspace_room(wst, stats):
         check(C, d, 1e-6, 128)
         C2 = torch.full_like(C, float("nan"))
         ws = wst.norm_workspace(A, B)
-        wst.wst_gemm_rmsnorm_bf16(A, B, C2, eps=1e-6, workspace=ws)        # N > 1024: the pass
+        wst.wst_gemm_rmsnorm_bf16(A, B, C2, eps=1e-6, workspace=ws)        # N > 2048: the pass
         assert wst.wst_sync_status(ws) == 0
         check(C2, d, 1e-6, 128)
 

@@ -360,11 +360,14 @@ long long stats_offset(int batch, int N, long strideB, bool layernorm) {
 
 // Statistics precomputed by a pass over A (NORM 3 / 4) or gathered in the
 // GEMM from the A tiles (NORM 1 / 2).  In the GEMM every tile recomputes its
-// rows' statistics, once per 256 columns of N; the pass reads A once more.
-// Measured on GB300 at 8192^3: RMSNorm 0.655 -> 0.617 ms, LayerNorm 0.751 ->
-// 0.646 ms with the pass.  Its extra read of A costs about as much as the
-// in-GEMM statistics of a 1024-column N, so the automatic choice takes the
-// pass for N > 1024 when the workspace holds the statistics.
+// rows' statistics, once per 256 columns of N; the pass reads A once more,
+// whose cost relative to the GEMM falls as 1/N.  Measured on GB300 (M 8192,
+// K 4096): LayerNorm's in-GEMM statistics (three operations per pair of
+// elements) lose from N = 1024 (0.0640 vs 0.0598 ms) and RMSNorm's (one)
+// only above N = 2048 (N = 2048: 0.0962 vs 0.0997 ms; 4096: 0.1640 vs
+// 0.1618 ms; 8192^3: 0.655 vs 0.617 ms).  So the automatic choice takes the
+// pass for N > 512 (LayerNorm) or N > 2048 (RMSNorm) when the workspace
+// holds the statistics.
 int choose_prestats(const GemmProblem& p, bool layernorm, size_t workspace_bytes, bool& pre) {
   const int opt = option_value(OPT_NORM_STATS);
   const long long need = stats_offset(p.batch, p.N, p.strideB, layernorm) +
@@ -373,7 +376,7 @@ int choose_prestats(const GemmProblem& p, bool layernorm, size_t workspace_bytes
   if (opt == 2 && !fits)
     return fail(WST_ERR_INVALID_ARG, "%s: precomputed statistics need a workspace of %lld bytes, %zu given",
                 layernorm ? "layernorm" : "rmsnorm", need, workspace_bytes);
-  pre = fits && (opt == 2 || (opt == 0 && p.N > 1024));
+  pre = fits && (opt == 2 || (opt == 0 && p.N > (layernorm ? 512 : 2048)));
   return WST_OK;
 }
 
