@@ -71,6 +71,22 @@ def test_grouped_edge_sizes(wst, sizes):
     assert torch.isnan(Cb[C.shape[0]:].float()).all()
 
 
+@pytest.mark.parametrize("G", [255, 300])
+def test_grouped_many_groups(wst, G):
+    # 255 groups: their 256 offsets fill the kernel's shared-memory offset
+    # table exactly; 300: past it, the tile walks read the offsets from
+    # global memory.  Small ragged groups, a third of them empty.
+    rng = np.random.default_rng(G)
+    sizes = rng.integers(1, 40, size=G)
+    sizes[rng.choice(G, size=G // 3, replace=False)] = 0
+    d = synthetic.grouped(experts=G, K=128, N=256, seed=G, group_sizes=sizes.tolist())
+    Cb, C, st = run_grouped(wst, d)
+    assert st == 0
+    ref = oracle.grouped(d["A"], d["B"], d["offsets"])
+    assert_parity(C, ref, 128, amax(d["A"]), amax(d["B"]), True, what="grouped many groups")
+    assert torch.isnan(Cb[C.shape[0]:].float()).all()
+
+
 def test_grouped_all_tokens_one_expert(wst):
     sizes = [0] * 7 + [700]
     d = synthetic.grouped(experts=8, K=256, N=256, seed=5, group_sizes=sizes)
